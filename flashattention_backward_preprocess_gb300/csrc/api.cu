@@ -1,0 +1,423 @@
+// api.cu -- the C ABI (include/fa.h): argument validation, the per
+// (device, stream) workspace cache and the launch sequence of each entry
+// point.  Validation mirrors the checks of boostr flash_bwd.rs
+// (flash_attention_bwd_impl: dout / output / lse shapes, contiguity, dtype,
+// window_size) and rustytorch backward.rs (flash_attention_backward: 4-D Q,
+// grad_output shape == Q shape, LSE shape) for what a C ABI of raw pointers
+// can check: pointers, sizes, alignment, dtype, scale, head dim.
+#include <math.h>
+#include <stdio.h>
+#include <stdlib.h>
+
+#include <map>
+#include <mutex>
+#include <vector>
+#include <string>
+#include <utility>
+
+#include "fa_internal.cuh"
+
+namespace fa {
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int status, const char* arg, const std::string& reason) {
+    g_last_error = std::string(arg) + ": " + reason;
+    return status;
+}
+
+int cuda_fail(const char* where, cudaError_t e) {
+    return fail(FA_ERR_CUDA, where, cudaGetErrorString(e));
+}
+
+bool debug_enabled() {
+    static int v = -1;
+    if (v < 0) {
+        const char* e = getenv("FA_DEBUG");
+        v = (e && *e && *e != '0') ? 1 : 0;
+    }
+    return v == 1;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int pad_rows(int S_q) { return (S_q + kTileQ - 1) / kTileQ * kTileQ; }
+
+struct WsLayout {
+    size_t off_err, off_lse2, off_D, off_dq, total;
+};
+
+WsLayout ws_layout(int B, int H, int S_q, int d) {
+    WsLayout L;
+    const size_t rows_pad = (size_t)B * H * pad_rows(S_q);
+    L.off_err = 0;
+    L.off_lse2 = 256;
+    L.off_D = align_up(L.off_lse2 + rows_pad * 4, 256);
+    L.off_dq = align_up(L.off_D + rows_pad * 4, 256);
+    L.total = align_up(L.off_dq + (size_t)B * H * S_q * d * 4, 256);
+    return L;
+}
+
+struct WsEntry {
+    void* base = nullptr;
+    size_t bytes = 0;
+};
+
+std::mutex g_ws_mu;
+std::map<std::pair<int, cudaStream_t>, WsEntry> g_ws;
+
+// Grow-only workspace of at least `bytes` for (current device, stream).
+int get_workspace(cudaStream_t st, size_t bytes, void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    WsEntry& w = g_ws[{dev, st}];
+    if (w.bytes < bytes) {
+        if (w.base) {
+            // the old buffer may still be in use by work queued on this stream
+            e = cudaStreamSynchronize(st);
+            if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
+            cudaFree(w.base);
+            w.base = nullptr;
+            w.bytes = 0;
+        }
+        void* p = nullptr;
+        e = cudaMalloc(&p, bytes);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(FA_ERR_NOMEM, "workspace", std::string("cudaMalloc failed: ") + cudaGetErrorString(e));
+        }
+        e = cudaMemsetAsync(p, 0, 256, st);  // error words
+        if (e != cudaSuccess) return cuda_fail("cudaMemsetAsync", e);
+        w.base = p;
+        w.bytes = bytes;
+    }
+    *out = w.base;
+    return FA_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_dims(int B, int H, int H_kv, int S_q, int S_k, int d, int dtype) {
+    if (B <= 0) return fail(FA_ERR_INVALID_ARG, "B", "must be > 0, got " + std::to_string(B));
+    if (H <= 0) return fail(FA_ERR_INVALID_ARG, "H", "must be > 0, got " + std::to_string(H));
+    if (H_kv <= 0) return fail(FA_ERR_INVALID_ARG, "H_kv", "must be > 0, got " + std::to_string(H_kv));
+    if (H % H_kv != 0)
+        return fail(FA_ERR_INVALID_ARG, "H_kv",
+                    "num_kv_heads " + std::to_string(H_kv) + " must divide num_heads " + std::to_string(H));
+    if (S_q <= 0) return fail(FA_ERR_INVALID_ARG, "S_q", "must be > 0, got " + std::to_string(S_q));
+    if (S_k <= 0) return fail(FA_ERR_INVALID_ARG, "S_k", "must be > 0, got " + std::to_string(S_k));
+    if (d <= 0) return fail(FA_ERR_INVALID_ARG, "d", "must be > 0, got " + std::to_string(d));
+    if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16)
+        return fail(FA_ERR_INVALID_ARG, "dtype", "unsupported dtype " + std::to_string(dtype) +
+                                                     " (expected FA_F32, FA_F16 or FA_BF16)");
+    if (d != 64 && d != 128)
+        return fail(FA_ERR_UNSUPPORTED, "d", "head dim " + std::to_string(d) + " not supported (64 or 128)");
+    // every flattened index must fit the kernels' 32-bit row arithmetic
+    const double rows_q = (double)B * H * (double)pad_rows(S_q);
+    const double rows_k = (double)B * H_kv * (double)S_k;
+    if (rows_q * d >= 9.0e18 || rows_q >= 2147483647.0 || rows_k >= 2147483647.0)
+        return fail(FA_ERR_INVALID_ARG, "shape", "tensor too large");
+    return FA_OK;
+}
+
+int check_scale(float scale) {
+    if (!(isfinite(scale) && scale > 0.f))
+        return fail(FA_ERR_INVALID_ARG, "scale", "must be finite and > 0");
+    return FA_OK;
+}
+
+int check_ptr(const void* p, const char* name, size_t align) {
+    if (p == nullptr) return fail(FA_ERR_INVALID_ARG, name, "null pointer");
+    if (!aligned(p, align))
+        return fail(FA_ERR_INVALID_ARG, name, "must be " + std::to_string(align) + "-byte aligned");
+    return FA_OK;
+}
+
+Shape make_shape(int B, int H, int H_kv, int S_q, int S_k, int d, float scale, int causal) {
+    Shape s;
+    s.B = B;
+    s.H = H;
+    s.H_kv = H_kv;
+    s.S_q = S_q;
+    s.S_k = S_k;
+    s.d = d;
+    s.scale = scale;
+    s.causal = causal ? 1 : 0;
+    s.S_q_pad = pad_rows(S_q);
+    return s;
+}
+
+// ---- optional per-kernel event timing (fa_profile)
+struct ProfRec {
+    cudaEvent_t ev[4];
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof_used;
+std::vector<ProfRec> g_prof_free;
+
+bool prof_begin(ProfRec* r) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (!g_prof_on) return false;
+    if (!g_prof_free.empty()) {
+        *r = g_prof_free.back();
+        g_prof_free.pop_back();
+        return true;
+    }
+    for (int i = 0; i < 4; ++i)
+        if (cudaEventCreate(&r->ev[i]) != cudaSuccess) return false;
+    return true;
+}
+void prof_end(const ProfRec& r) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof_used.push_back(r);
+}
+
+bool use_simt_for_16bit() {
+    static int v = -1;
+    if (v < 0) {
+        const char* e = getenv("FA_BWD_KERNEL");
+        v = (e && std::string(e) == "simt") ? 1 : 0;
+    }
+    return v == 1;
+}
+
+int bwd_impl(const void* dO, const void* Q, const void* K, const void* V, const void* O,
+             const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv, int S_q,
+             int S_k, int d, float scale, int causal, int dtype, cudaStream_t st) {
+    int rc;
+    if ((rc = check_dims(B, H, H_kv, S_q, S_k, d, dtype))) return rc;
+    if ((rc = check_scale(scale))) return rc;
+    if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal", "must be 0 or 1");
+    if ((rc = check_ptr(dO, "dO", 16)) || (rc = check_ptr(Q, "Q", 16)) || (rc = check_ptr(K, "K", 16)) ||
+        (rc = check_ptr(V, "V", 16)) || (rc = check_ptr(O, "O", 16)) || (rc = check_ptr(LSE, "LSE", 4)) ||
+        (rc = check_ptr(dQ, "dQ", 16)) || (rc = check_ptr(dK, "dK", 16)) || (rc = check_ptr(dV, "dV", 16)))
+        return rc;
+    const Shape s = make_shape(B, H, H_kv, S_q, S_k, d, scale, causal);
+    const WsLayout L = ws_layout(B, H, S_q, d);
+    void* base = nullptr;
+    if ((rc = get_workspace(st, L.total, &base))) return rc;
+    Workspace ws;
+    ws.err = reinterpret_cast<unsigned int*>(static_cast<char*>(base) + L.off_err);
+    ws.lse2 = reinterpret_cast<float*>(static_cast<char*>(base) + L.off_lse2);
+    ws.Dws = reinterpret_cast<float*>(static_cast<char*>(base) + L.off_D);
+    ws.dqacc = reinterpret_cast<float*>(static_cast<char*>(base) + L.off_dq);
+    const bool tc = dtype != FA_F32 && !use_simt_for_16bit();
+    if (debug_enabled())
+        fprintf(stderr,
+                "[fa] bwd B=%d H=%d H_kv=%d S_q=%d S_k=%d d=%d causal=%d dtype=%d kernel=%s grid=%d ws=%zu\n",
+                B, H, H_kv, S_q, S_k, d, causal, dtype, tc ? "sm103" : "simt",
+                tc ? (S_k + kTileK - 1) / kTileK * B * H_kv : 0, L.total);
+    ProfRec pr;
+    const bool prof = prof_begin(&pr);
+    if (prof) cudaEventRecord(pr.ev[0], st);
+    cudaError_t e = launch_preprocess(dtype, dO, O, LSE, ws.Dws, ws.lse2, ws.dqacc, s, s.S_q_pad, st);
+    if (e != cudaSuccess) return cuda_fail("preprocess launch", e);
+    if (prof) cudaEventRecord(pr.ev[1], st);
+    e = tc ? launch_bwd_sm103(dtype, Q, K, V, dO, ws, dK, dV, s, st)
+           : launch_bwd_simt(dtype, Q, K, V, dO, ws, dK, dV, s, st);
+    if (e != cudaSuccess) return cuda_fail("main kernel launch", e);
+    if (prof) cudaEventRecord(pr.ev[2], st);
+    e = launch_dq_finalize(dtype, ws.dqacc, dQ, s, st);
+    if (e != cudaSuccess) return cuda_fail("dq finalize launch", e);
+    if (prof) {
+        cudaEventRecord(pr.ev[3], st);
+        prof_end(pr);
+    }
+    return FA_OK;
+}
+
+size_t elem_size(int dtype) { return dtype == FA_F32 ? 4 : 2; }
+
+// Host-buffer staging for fa_bwd_host, per (device, stream).
+struct HostStage {
+    void* base = nullptr;
+    size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, HostStage> g_stage;
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_bwd(const void* dO, const void* Q, const void* K, const void* V, const void* O,
+           const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv, int S_q,
+           int S_k, int d, float scale, int causal, int dtype, void* stream) {
+    g_last_error.clear();
+    return bwd_impl(dO, Q, K, V, O, LSE, dQ, dK, dV, B, H, H_kv, S_q, S_k, d, scale, causal, dtype,
+                    static_cast<cudaStream_t>(stream));
+}
+
+int fa_bwd_preprocess(const void* dO, const void* O, float* D, int B, int H, int S_q, int d,
+                      int dtype, void* stream) {
+    g_last_error.clear();
+    int rc;
+    if ((rc = check_dims(B, H, H, S_q, 1, d, dtype))) return rc;
+    if ((rc = check_ptr(dO, "dO", 16)) || (rc = check_ptr(O, "O", 16)) || (rc = check_ptr(D, "D", 4)))
+        return rc;
+    const Shape s = make_shape(B, H, H, S_q, 1, d, 1.f, 0);
+    cudaError_t e = launch_preprocess(dtype, dO, O, nullptr, D, nullptr, nullptr, s, S_q,
+                                      static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail("preprocess launch", e);
+    return FA_OK;
+}
+
+int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+           int H_kv, int S_q, int S_k, int d, float scale, int causal, int dtype, void* stream) {
+    g_last_error.clear();
+    int rc;
+    if ((rc = check_dims(B, H, H_kv, S_q, S_k, d, dtype))) return rc;
+    if ((rc = check_scale(scale))) return rc;
+    if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal", "must be 0 or 1");
+    if ((rc = check_ptr(Q, "Q", 16)) || (rc = check_ptr(K, "K", 16)) || (rc = check_ptr(V, "V", 16)) ||
+        (rc = check_ptr(O, "O", 16)) || (rc = check_ptr(LSE, "LSE", 4)))
+        return rc;
+    const Shape s = make_shape(B, H, H_kv, S_q, S_k, d, scale, causal);
+    cudaError_t e = launch_fwd_simt(dtype, Q, K, V, O, LSE, s, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail("forward launch", e);
+    return FA_OK;
+}
+
+int fa_bwd_host(const void* dO, const void* Q, const void* K, const void* V, const void* O,
+                const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv, int S_q,
+                int S_k, int d, float scale, int causal, int dtype, void* stream) {
+    g_last_error.clear();
+    int rc;
+    if ((rc = check_dims(B, H, H_kv, S_q, S_k, d, dtype))) return rc;
+    if ((rc = check_ptr(dO, "dO", 1)) || (rc = check_ptr(Q, "Q", 1)) || (rc = check_ptr(K, "K", 1)) ||
+        (rc = check_ptr(V, "V", 1)) || (rc = check_ptr(O, "O", 1)) || (rc = check_ptr(LSE, "LSE", 1)) ||
+        (rc = check_ptr(dQ, "dQ", 1)) || (rc = check_ptr(dK, "dK", 1)) || (rc = check_ptr(dV, "dV", 1)))
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t es = elem_size(dtype);
+    const size_t nq = (size_t)B * H * S_q * d * es, nk = (size_t)B * H_kv * S_k * d * es;
+    const size_t nl = (size_t)B * H * S_q * 4;
+    // device layout: dO Q O dQ | K V dK dV | LSE, each 256-byte aligned
+    size_t off[9], tot = 0;
+    const size_t sz[9] = {nq, nq, nq, nq, nk, nk, nk, nk, nl};
+    for (int i = 0; i < 9; ++i) {
+        off[i] = tot;
+        tot = align_up(tot + sz[i], 256);
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+    char* dbase = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_ws_mu);
+        HostStage& hs = g_stage[{dev, st}];
+        if (hs.bytes < tot) {
+            if (hs.base) {
+                cudaStreamSynchronize(st);
+                cudaFree(hs.base);
+                hs.base = nullptr;
+                hs.bytes = 0;
+            }
+            e = cudaMalloc(&hs.base, tot);
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                hs.base = nullptr;
+                return fail(FA_ERR_NOMEM, "staging", cudaGetErrorString(e));
+            }
+            hs.bytes = tot;
+        }
+        dbase = static_cast<char*>(hs.base);
+    }
+    const void* hin[6] = {dO, Q, O, K, V, LSE};
+    const int in_slot[6] = {0, 1, 2, 4, 5, 8};
+    for (int i = 0; i < 6; ++i) {
+        e = cudaMemcpyAsync(dbase + off[in_slot[i]], hin[i], sz[in_slot[i]], cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) return cuda_fail("cudaMemcpyAsync H2D", e);
+    }
+    rc = bwd_impl(dbase + off[0], dbase + off[1], dbase + off[4], dbase + off[5], dbase + off[2],
+                  reinterpret_cast<const float*>(dbase + off[8]), dbase + off[3], dbase + off[6],
+                  dbase + off[7], B, H, H_kv, S_q, S_k, d, scale, causal, dtype, st);
+    if (rc != FA_OK) return rc;
+    void* hout[3] = {dQ, dK, dV};
+    const int out_slot[3] = {3, 6, 7};
+    for (int i = 0; i < 3; ++i) {
+        e = cudaMemcpyAsync(hout[i], dbase + off[out_slot[i]], sz[out_slot[i]], cudaMemcpyDeviceToHost, st);
+        if (e != cudaSuccess) return cuda_fail("cudaMemcpyAsync D2H", e);
+    }
+    e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
+    return FA_OK;
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int S_q, int d) {
+    if (B <= 0 || H <= 0 || S_q <= 0 || d <= 0) return 0;
+    return ws_layout(B, H, S_q, d).total;
+}
+
+int fa_check_device(void* stream) {
+    g_last_error.clear();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+    void* base = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_ws_mu);
+        auto it = g_ws.find({dev, st});
+        if (it == g_ws.end()) return FA_OK;
+        base = it->second.base;
+    }
+    unsigned int words[4] = {0, 0, 0, 0};
+    e = cudaMemcpy(words, base, sizeof(words), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail("cudaMemcpy", e);
+    if (words[0] == 0) return FA_OK;
+    cudaMemset(base, 0, sizeof(words));
+    if (words[0] & kErrTimeout) return fail(FA_ERR_TIMEOUT, "device", "a bounded wait in a kernel timed out");
+    return fail(FA_ERR_CUDA, "device", "kernel error word " + std::to_string(words[0]));
+}
+
+int fa_profile(int enable) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    for (auto& r : g_prof_used) g_prof_free.push_back(r);
+    g_prof_used.clear();
+    g_prof_on = enable != 0;
+    return FA_OK;
+}
+
+int fa_profile_read(float* ms, int* calls) {
+    g_last_error.clear();
+    if (ms == nullptr || calls == nullptr) return fail(FA_ERR_INVALID_ARG, "ms", "null pointer");
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    ms[0] = ms[1] = ms[2] = 0.f;
+    for (auto& r : g_prof_used) {
+        cudaError_t e = cudaEventSynchronize(r.ev[3]);
+        if (e != cudaSuccess) return cuda_fail("cudaEventSynchronize", e);
+        for (int k = 0; k < 3; ++k) {
+            float t = 0.f;
+            e = cudaEventElapsedTime(&t, r.ev[k], r.ev[k + 1]);
+            if (e != cudaSuccess) return cuda_fail("cudaEventElapsedTime", e);
+            ms[k] += t;
+        }
+    }
+    *calls = (int)g_prof_used.size();
+    return FA_OK;
+}
+
+const char* fa_last_error(void) { return g_last_error.c_str(); }
+
+void fa_shutdown(void) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    for (auto& kv : g_ws)
+        if (kv.second.base) cudaFree(kv.second.base);
+    g_ws.clear();
+    for (auto& kv : g_stage)
+        if (kv.second.base) cudaFree(kv.second.base);
+    g_stage.clear();
+}
+
+const char* fa_version(void) { return "fa-gb300 0.1.0 (sm_103a)"; }
+
+}  // extern "C"

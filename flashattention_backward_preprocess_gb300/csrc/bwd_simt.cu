@@ -1,0 +1,154 @@
+// bwd_simt.cu -- CUDA-core (FFMA) main backward kernel, used for fp32
+// inputs.  fp32 needs the 1e-4 relative tolerance, which tf32 tensor-core
+// operands (10-bit mantissa) would not meet, and the fp32 workloads are small,
+// so this kernel favours plain, checkable arithmetic over speed.
+//
+// Work split (same math as the tensor-core kernel): one CTA owns a tile of
+// kTile key/value rows of one (batch, kv head), keeps its dK / dV rows in
+// shared memory, and walks every query row of every query head in the group:
+//   S_ij = <Q_i, K_j>,  P_ij = exp(scale * S_ij - LSE_i)   (masked -> 0)
+//   dP_ij = <dO_i, V_j>, dS_ij = P_ij * (dP_ij - D_i)
+//   dV_j += P_ij dO_i,   dK_j += dS_ij Q_i,   dQacc_i += sum_j dS_ij K_j (atomic)
+// scale is applied to dK here and to dQ in the finalisation kernel.
+#include <math.h>
+
+#include "fa_internal.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kTile = 32;      // key rows per CTA
+constexpr int kThreads = 128;  // 4 warps
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) bwd_simt_kernel(
+    const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
+    const T* __restrict__ dO, const float* __restrict__ lse2, const float* __restrict__ Dws,
+    float* __restrict__ dqacc, T* __restrict__ dK, T* __restrict__ dV, Shape s) {
+    extern __shared__ float smem[];
+    float* sK = smem;                 // [kTile][D]
+    float* sV = sK + kTile * D;       // [kTile][D]
+    float* sdK = sV + kTile * D;      // [kTile][D]
+    float* sdV = sdK + kTile * D;     // [kTile][D]
+    float* sq = sdV + kTile * D;      // [D]
+    float* sdo = sq + D;              // [D]
+    float* sp = sdo + D;              // [kTile]
+    float* sds = sp + kTile;          // [kTile]
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int n0 = blockIdx.x * kTile;
+    const int bkv = blockIdx.y;  // b * H_kv + hk
+    const int b = bkv / s.H_kv, hk = bkv % s.H_kv;
+    const int g = s.H / s.H_kv;
+    const int off = s.S_k - s.S_q;  // causal: key j visible to query i iff j <= i + off
+    const float kLog2e = 1.4426950408889634f;
+
+    for (int e = tid; e < kTile * D; e += kThreads) {
+        const int j = e / D, c = e % D;
+        const int jj = n0 + j;
+        const size_t gi = ((size_t)bkv * s.S_k + jj) * D + c;
+        sK[e] = jj < s.S_k ? TypeTraits<T>::to_f32(K[gi]) : 0.f;
+        sV[e] = jj < s.S_k ? TypeTraits<T>::to_f32(V[gi]) : 0.f;
+        sdK[e] = 0.f;
+        sdV[e] = 0.f;
+    }
+    __syncthreads();
+
+    // first query row that can see a key of this tile
+    int i_begin = 0;
+    if (s.causal) i_begin = max(0, n0 - off);
+
+    for (int h = hk * g; h < (hk + 1) * g; ++h) {
+        const int bh = b * s.H + h;
+        for (int i = i_begin; i < s.S_q; ++i) {
+            const size_t qi = ((size_t)bh * s.S_q + i) * D;
+            for (int c = tid; c < D; c += kThreads) {
+                sq[c] = TypeTraits<T>::to_f32(Q[qi + c]);
+                sdo[c] = TypeTraits<T>::to_f32(dO[qi + c]);
+            }
+            __syncthreads();
+            const float l2 = lse2[(size_t)bh * s.S_q_pad + i];
+            const float Di = Dws[(size_t)bh * s.S_q_pad + i];
+            for (int r = 0; r < kTile / 4; ++r) {
+                const int j = warp * (kTile / 4) + r;
+                float sd = 0.f, dp = 0.f;
+                for (int c = lane; c < D; c += 32) {
+                    sd = fmaf(sq[c], sK[j * D + c], sd);
+                    dp = fmaf(sdo[c], sV[j * D + c], dp);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    sd += __shfl_xor_sync(0xffffffffu, sd, o);
+                    dp += __shfl_xor_sync(0xffffffffu, dp, o);
+                }
+                if (lane == 0) {
+                    const int jj = n0 + j;
+                    const bool vis = jj < s.S_k && (!s.causal || jj <= i + off);
+                    // exp(scale*S - LSE) = exp2(scale*log2e*S - LSE*log2e)
+                    const float p = vis ? exp2f(fmaf(sd, s.scale * kLog2e, -l2)) : 0.f;
+                    sp[j] = p;
+                    sds[j] = p * (dp - Di);
+                }
+            }
+            __syncthreads();
+            for (int c = tid; c < D; c += kThreads) {
+                float acc = 0.f;
+                const float qc = sq[c], doc = sdo[c];
+#pragma unroll 8
+                for (int j = 0; j < kTile; ++j) {
+                    sdV[j * D + c] = fmaf(sp[j], doc, sdV[j * D + c]);
+                    sdK[j * D + c] = fmaf(sds[j], qc, sdK[j * D + c]);
+                    acc = fmaf(sds[j], sK[j * D + c], acc);
+                }
+                atomicAdd(dqacc + qi + c, acc);
+            }
+            __syncthreads();
+        }
+    }
+    for (int e = tid; e < kTile * D; e += kThreads) {
+        const int j = e / D, c = e % D;
+        const int jj = n0 + j;
+        if (jj < s.S_k) {
+            const size_t gi = ((size_t)bkv * s.S_k + jj) * D + c;
+            dK[gi] = TypeTraits<T>::from_f32(sdK[e] * s.scale);
+            dV[gi] = TypeTraits<T>::from_f32(sdV[e]);
+        }
+    }
+}
+
+template <typename T, int D>
+cudaError_t launch_t(const void* Q, const void* K, const void* V, const void* dO,
+                     const Workspace& ws, void* dK, void* dV, const Shape& s, cudaStream_t st) {
+    const size_t smem = sizeof(float) * (4 * kTile * D + 2 * D + 2 * kTile);
+    auto kern = bwd_simt_kernel<T, D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((s.S_k + kTile - 1) / kTile, s.B * s.H_kv);
+    kern<<<grid, kThreads, smem, st>>>(static_cast<const T*>(Q), static_cast<const T*>(K),
+                                       static_cast<const T*>(V), static_cast<const T*>(dO),
+                                       ws.lse2, ws.Dws, ws.dqacc, static_cast<T*>(dK),
+                                       static_cast<T*>(dV), s);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_simt(int dtype, const void* Q, const void* K, const void* V,
+                            const void* dO, const Workspace& ws, void* dK, void* dV,
+                            const Shape& s, cudaStream_t st) {
+#define FA_L(T, DD) return launch_t<T, DD>(Q, K, V, dO, ws, dK, dV, s, st)
+    if (s.d == 64) {
+        if (dtype == FA_F32) FA_L(float, 64);
+        if (dtype == FA_F16) FA_L(__half, 64);
+        if (dtype == FA_BF16) FA_L(__nv_bfloat16, 64);
+    } else if (s.d == 128) {
+        if (dtype == FA_F32) FA_L(float, 128);
+        if (dtype == FA_F16) FA_L(__half, 128);
+        if (dtype == FA_BF16) FA_L(__nv_bfloat16, 128);
+    }
+#undef FA_L
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

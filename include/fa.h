@@ -1,0 +1,149 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) FlashAttention-2 backward library.
+ *
+ * Operation (FlashAttention-2 backward as described by boostr 0.1.0,
+ * src/ops/cuda/attention/flash_bwd.rs, doc comment of
+ * flash_attention_bwd_impl, "Two-step process"):
+ *   step 1 (preprocess)  D_i   = sum_c dO_ic * O_ic              (fp32)
+ *   step 2 (main)        P_ij  = exp(scale * <Q_i, K_j> - LSE_i)  (masked -> 0)
+ *                        dV_j  = sum_i P_ij dO_i
+ *                        dS_ij = P_ij * (<dO_i, V_j> - D_i)
+ *                        dK_j  = scale * sum_i dS_ij Q_i
+ *                        dQ_i  = scale * sum_j dS_ij K_j
+ * dK and dV of a key/value head are summed over the H / H_kv query heads
+ * that share it; query head h uses key/value head h / (H / H_kv).
+ * Causal masking keeps key j for query i iff j <= i + (S_k - S_q).
+ *
+ * Layouts (shape checks of flash_attention_bwd_impl in flash_bwd.rs and of
+ * flash_attention_backward in rustytorch rtx-flash-metal-attention
+ * backward.rs): every tensor is dense row-major,
+ *   Q, O, dO, dQ : [B, H,    S_q, d]   element type `dtype`
+ *   K, V, dK, dV : [B, H_kv, S_k, d]   element type `dtype`
+ *   LSE, D       : [B, H,    S_q]      float32, natural-log log-sum-exp of
+ *                                      the scaled scores (-inf for a row
+ *                                      that sees no key)
+ *
+ * Pointers are DEVICE pointers unless an entry point says otherwise.  The
+ * caller owns every buffer it passes; the library owns an internal workspace
+ * (fp32 dQ accumulator, D and a padded copy of LSE) cached per
+ * (device, stream) and released by fa_shutdown().  All calls are
+ * asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream):
+ * they return after enqueueing, results are valid in stream order, inputs
+ * are never modified and outputs are fully overwritten.
+ *
+ * Errors: every entry point returns an fa_status.  Argument errors are
+ * detected on the host before anything is enqueued (FA_ERR_INVALID_ARG /
+ * FA_ERR_UNSUPPORTED) and fa_last_error() then names the argument and the
+ * reason, like the InvalidArgument { arg, reason } errors of flash_bwd.rs.
+ * CUDA launch failures give FA_ERR_CUDA.  Device-side waits are bounded: a
+ * kernel whose wait runs out records it in the workspace error word and
+ * returns; fa_check_device(stream) reports it as FA_ERR_TIMEOUT.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { FA_F32 = 0, FA_F16 = 1, FA_BF16 = 2 } fa_dtype;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1, /* bad pointer, shape, dtype, scale or alignment */
+    FA_ERR_UNSUPPORTED = 2, /* valid but not implemented (head dim not 64 / 128) */
+    FA_ERR_CUDA = 3,        /* a CUDA runtime / driver call failed */
+    FA_ERR_TIMEOUT = 4,     /* a device-side bounded wait ran out */
+    FA_ERR_NOMEM = 5        /* workspace allocation failed */
+} fa_status;
+
+/*
+ * fa_bwd -- full FlashAttention-2 backward: preprocess D, then dQ, dK, dV.
+ *   dO, Q, O      : [B, H, S_q, d]  dtype, 16-byte aligned
+ *   K, V          : [B, H_kv, S_k, d] dtype, 16-byte aligned
+ *   LSE           : [B, H, S_q] float32, 4-byte aligned
+ *   dQ            : [B, H, S_q, d]  dtype, written
+ *   dK, dV        : [B, H_kv, S_k, d] dtype, written (rows no query sees get 0)
+ *   B, H, H_kv, S_q, S_k > 0, H % H_kv == 0, d in {64, 128}
+ *   scale         : finite, > 0 (usually 1/sqrt(d))
+ *   causal        : 0 or 1
+ *   dtype         : fa_dtype (F32, F16, BF16); accumulation is fp32
+ *   stream        : cudaStream_t
+ * F16/BF16 run the tcgen05 tensor-core kernel; F32 runs an FFMA kernel.
+ * dQ is reduced across key tiles with fp32 atomics, so dQ may differ in the
+ * last bits between runs (flash_bwd.rs, "dQ must be zeroed -- backward uses
+ * atomicAdd"); dK and dV are deterministic.
+ */
+int fa_bwd(const void* dO, const void* Q, const void* K, const void* V, const void* O,
+           const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv, int S_q,
+           int S_k, int d, float scale, int causal, int dtype, void* stream);
+
+/*
+ * fa_bwd_preprocess -- step 1 alone (flash_bwd.rs, "Step 1: Preprocessing --
+ * compute D = rowsum(dO (.) O) per query position"):
+ *   D[b, h, i] = sum_c dO[b, h, i, c] * O[b, h, i, c], accumulated in fp32.
+ *   dO, O : [B, H, S_q, d] dtype, 16-byte aligned;  D : [B, H, S_q] float32.
+ */
+int fa_bwd_preprocess(const void* dO, const void* O, float* D, int B, int H, int S_q, int d,
+                      int dtype, void* stream);
+
+/*
+ * fa_fwd -- attention forward helper producing the O and LSE the backward
+ * consumes (boostr autograd_attention.rs, var_flash_attention saves
+ * q, k, v, output, lse):  O_i = sum_j softmax_j(scale <Q_i, K_j>) V_j and
+ * LSE_i = log sum_j exp(scale <Q_i, K_j>) over the visible keys.
+ *   Q : [B, H, S_q, d], K, V : [B, H_kv, S_k, d], O : [B, H, S_q, d] dtype;
+ *   LSE : [B, H, S_q] float32.  Rows that see no key get O = 0, LSE = -inf.
+ * A correctness helper computed with CUDA-core fp32 arithmetic.
+ */
+int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+           int H_kv, int S_q, int S_k, int d, float scale, int causal, int dtype, void* stream);
+
+/*
+ * fa_bwd_host -- fa_bwd on HOST buffers (same arguments and layouts, every
+ * pointer a host pointer; pinned memory gives full copy bandwidth).  Copies
+ * the inputs to device buffers cached per (device, stream), runs fa_bwd on
+ * `stream`, copies dQ, dK, dV back and synchronizes `stream` before
+ * returning.
+ */
+int fa_bwd_host(const void* dO, const void* Q, const void* K, const void* V, const void* O,
+                const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv, int S_q,
+                int S_k, int d, float scale, int causal, int dtype, void* stream);
+
+/* Workspace bytes fa_bwd needs for a shape (informational; the library
+ * allocates and caches it itself). */
+size_t fa_bwd_workspace_bytes(int B, int H, int S_q, int d);
+
+/* Synchronizes `stream`, then returns FA_ERR_TIMEOUT if a kernel of this
+ * library on that stream recorded a bounded-wait timeout since the last
+ * check (clearing the record), else FA_OK (or FA_ERR_CUDA). */
+int fa_check_device(void* stream);
+
+/*
+ * Per-kernel timing of fa_bwd calls (CUDA events recorded on the caller's
+ * stream around each of the three launches: preprocess, main, dQ finalise).
+ * fa_profile(1) clears the record and starts collecting, fa_profile(0)
+ * stops.  fa_profile_read synchronizes on the recorded events and returns
+ * the summed milliseconds per kernel in ms[0..2] and the number of fa_bwd
+ * calls recorded.  Recording adds event records to the stream, nothing else.
+ */
+int fa_profile(int enable);
+int fa_profile_read(float* ms, int* calls);
+
+/* Thread-local text of the last error ("arg: reason"); "" if none. */
+const char* fa_last_error(void);
+
+/* Frees every cached workspace of the calling process (all devices).  Must
+ * not race with calls in flight. */
+void fa_shutdown(void);
+
+/* Library version string. */
+const char* fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */
