@@ -143,6 +143,30 @@ def max_over_ranks(x: float, world: int, device) -> float:
     return float(t.item())
 
 
+def kernel_source_hash() -> str:
+    """Hash of the main kernel's sources: ncu traffic counters are only valid for this exact kernel."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("bwd_sm103.cu", "sm103_ptx.cuh", "fa_internal.cuh"):
+        with open(os.path.join(ROOT, "flashattention_backward_preprocess_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def main_kernel_traffic(workload: str):
+    """DRAM bytes (read + write) per main-kernel launch from the committed ncu summary, or None
+    when the kernel's sources changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("kernel_sha") != kernel_source_hash():
+        return None
+    return d.get("bytes_per_launch", {}).get(workload)
+
+
 def workload_config(w, extra=None):
     cfg = {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.H_kv, "S_q": w.S_q, "S_k": w.S_k,
            "d": w.d, "causal": w.causal, "scale": "1/sqrt(d)", "dtype": w.dtype,
@@ -271,13 +295,7 @@ def main():
     main_ms = ms_main / max(calls, 1)
     achieved = flops / (main_ms / 1e3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    traffic = None
-    prof_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof_path):
-        try:
-            traffic = json.load(open(prof_path)).get(w.name)
-        except Exception:
-            traffic = None
+    traffic = main_kernel_traffic(w.name)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic, "peak_source": f"{peak_src} bf16_tflops (burst)",
                 "kernel": "bwd_sm103_kernel<bf16,128>", "kernel_ms": main_ms,

@@ -15,6 +15,7 @@ from .binding import (  # noqa: F401
     FaError,
     fa_bwd,
     fa_bwd_host,
+    fa_bwd_noalloc,
     fa_bwd_preprocess,
     fa_bwd_workspace_bytes,
     fa_check_device,

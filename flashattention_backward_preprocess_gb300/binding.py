@@ -27,7 +27,7 @@ _lock = threading.Lock()
 _lib = None
 
 #: every symbol include/fa.h declares
-EXPORTS = ("fa_bwd", "fa_bwd_preprocess", "fa_fwd", "fa_bwd_host", "fa_bwd_workspace_bytes",
+EXPORTS = ("fa_bwd", "fa_bwd_noalloc", "fa_bwd_preprocess", "fa_fwd", "fa_bwd_host", "fa_bwd_workspace_bytes",
            "fa_check_device", "fa_profile", "fa_profile_read", "fa_last_error", "fa_shutdown",
            "fa_version")
 
@@ -56,6 +56,8 @@ def load_library(path: str | None = None):
         big = [V] * 9 + [I] * 6 + [F, I, I, V]
         lib.fa_bwd.argtypes = big
         lib.fa_bwd.restype = I
+        lib.fa_bwd_noalloc.argtypes = big
+        lib.fa_bwd_noalloc.restype = I
         lib.fa_bwd_host.argtypes = big
         lib.fa_bwd_host.restype = I
         lib.fa_bwd_preprocess.argtypes = [V, V, V, I, I, I, I, I, V]
@@ -167,6 +169,20 @@ def fa_bwd(dO, Q, K, V, O, LSE, scale: float | None = None, causal: bool = False
         _check(load_library().fa_bwd(_ptr(dO), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE),
                                      _ptr(dQ), _ptr(dK), _ptr(dV), B, H, H_kv, S_q, S_k, d, scale,
                                      int(bool(causal)), _dtype(Q), _stream(stream)))
+    return dQ, dK, dV
+
+
+def fa_bwd_noalloc(dO, Q, K, V, O, LSE, dQ, dK, dV, scale: float | None = None,
+                   causal: bool = False, stream=None):
+    """fa_bwd without any device allocation by the library (fixed 32 MiB scratch);
+    outputs must be passed in.  See include/fa.h (fa_bwd_noalloc)."""
+    B, H, H_kv, S_q, S_k, d = _dims(Q, K)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dev = _on_device((dO, Q, K, V, O, LSE, dQ, dK, dV))
+    with torch.cuda.device(dev):
+        _check(load_library().fa_bwd_noalloc(_ptr(dO), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE),
+                                             _ptr(dQ), _ptr(dK), _ptr(dV), B, H, H_kv, S_q, S_k, d,
+                                             scale, int(bool(causal)), _dtype(Q), _stream(stream)))
     return dQ, dK, dV
 
 

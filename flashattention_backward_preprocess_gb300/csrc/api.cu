@@ -240,6 +240,26 @@ struct HostStage {
 std::map<std::pair<int, cudaStream_t>, HostStage> g_stage;
 
 }  // namespace
+
+// Argument checks of fa_bwd, shared with the other backward entry points.
+int validate_bwd_args(const void* dO, const void* Q, const void* K, const void* V, const void* O,
+                      const float* LSE, const void* dQ, const void* dK, const void* dV, int B, int H,
+                      int H_kv, int S_q, int S_k, int d, float scale, int causal, int dtype) {
+    int rc;
+    if ((rc = check_dims(B, H, H_kv, S_q, S_k, d, dtype))) return rc;
+    if ((rc = check_scale(scale))) return rc;
+    if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal", "must be 0 or 1");
+    if ((rc = check_ptr(dO, "dO", 16)) || (rc = check_ptr(Q, "Q", 16)) || (rc = check_ptr(K, "K", 16)) ||
+        (rc = check_ptr(V, "V", 16)) || (rc = check_ptr(O, "O", 16)) || (rc = check_ptr(LSE, "LSE", 4)) ||
+        (rc = check_ptr(dQ, "dQ", 16)) || (rc = check_ptr(dK, "dK", 16)) || (rc = check_ptr(dV, "dV", 16)))
+        return rc;
+    return FA_OK;
+}
+
+int set_error(int status, const char* arg, const char* reason) { return fail(status, arg, reason); }
+
+void clear_error() { g_last_error.clear(); }
+
 }  // namespace fa
 
 using namespace fa;

@@ -73,4 +73,11 @@ cudaError_t launch_bwd_sm103(int dtype, const void* Q, const void* K, const void
                              const void* dO, const Workspace& ws, void* dK, void* dV,
                              const Shape& s, cudaStream_t st);
 
+// api.cu: argument checks and error text shared by the entry points.
+int validate_bwd_args(const void* dO, const void* Q, const void* K, const void* V, const void* O,
+                      const float* LSE, const void* dQ, const void* dK, const void* dV, int B, int H,
+                      int H_kv, int S_q, int S_k, int d, float scale, int causal, int dtype);
+int set_error(int status, const char* arg, const char* reason);
+void clear_error();
+
 }  // namespace fa

@@ -1,0 +1,124 @@
+// noalloc.cu -- fa_bwd_noalloc: the full backward (preprocess, main kernel,
+// dQ finalise) for callers that must not allocate device memory.
+//
+// fa_bwd keeps its scratch (fp32 dQ accumulator, D, padded LSE copy, error
+// words) in a workspace it allocates with cudaMalloc on first use.  Some
+// callers cannot allow that: code running under a memory pool or allocator
+// that owns all device memory, hosts whose allocation calls would
+// synchronize the device at a bad moment, or runtimes that forbid the library
+// from allocating on its own.  This entry point instead uses one fixed
+// scratch array compiled into the library (g_fa_noalloc_scratch below), so a
+// call only launches kernels.
+//
+// Rules for users:
+//   * The array is kFaNoallocScratchBytes (32 MiB) on every GPU that loads the
+//     library, held until the process exits.  A shape needs
+//       256 + 2 * 4 * B*H*ceil(S_q/128)*128 + 4 * B*H*S_q*d   bytes
+//     (each part rounded up to 256); larger shapes are rejected with
+//     FA_ERR_INVALID_ARG ("scratch: ...") and nothing is launched.
+//   * The first call on a device looks up the array's device address
+//     (cudaGetSymbolAddress) and clears its error words; make that first call
+//     before any stream capture.
+//   * All calls share the one array and it keeps the last call's contents;
+//     every call re-zeroes the parts that must start at zero.  Calls whose GPU
+//     work overlaps (other streams, other host threads) race on it: order them
+//     on one stream.
+//   * Device-side bounded-wait timeouts of this variant are recorded in the
+//     array's first word, which fa_check_device does not read.
+#include <stdio.h>
+
+#include <mutex>
+
+#include "fa_internal.cuh"
+
+namespace {
+constexpr size_t kFaNoallocScratchBytes = 32u << 20;
+constexpr int kFaMaxDevices = 64;
+}  // namespace
+
+// The scratch itself.  In host code this name is only a stand-in for the
+// device symbol: never pass it to a kernel, use the address looked up below.
+static __device__ __align__(256) unsigned char g_fa_noalloc_scratch[kFaNoallocScratchBytes];
+
+namespace fa {
+namespace {
+
+std::mutex g_na_mu;
+void* g_na_ptr[kFaMaxDevices] = {};
+
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Device address of the scratch array on the current device (set-up once per device).
+int scratch_address(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return set_error(FA_ERR_CUDA, "cudaGetDevice", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kFaMaxDevices) return set_error(FA_ERR_UNSUPPORTED, "device", "device index too large");
+    std::lock_guard<std::mutex> lk(g_na_mu);
+    if (g_na_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_fa_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr)
+            return set_error(FA_ERR_CUDA, "cudaGetSymbolAddress", cudaGetErrorString(e));
+        e = cudaMemset(p, 0, 256);  // error words
+        if (e != cudaSuccess) return set_error(FA_ERR_CUDA, "cudaMemset", cudaGetErrorString(e));
+        g_na_ptr[dev] = p;
+    }
+    *out = g_na_ptr[dev];
+    return FA_OK;
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" int fa_bwd_noalloc(const void* dO, const void* Q, const void* K, const void* V,
+                              const void* O, const float* LSE, void* dQ, void* dK, void* dV, int B,
+                              int H, int H_kv, int S_q, int S_k, int d, float scale, int causal,
+                              int dtype, void* stream) {
+    clear_error();
+    int rc = validate_bwd_args(dO, Q, K, V, O, LSE, dQ, dK, dV, B, H, H_kv, S_q, S_k, d, scale, causal,
+                               dtype);
+    if (rc != FA_OK) return rc;
+    const int S_q_pad = (S_q + kTileQ - 1) / kTileQ * kTileQ;
+    const size_t rows_pad = (size_t)B * H * S_q_pad;
+    const size_t off_lse2 = 256;
+    const size_t off_D = off_lse2 + up256(rows_pad * 4);
+    const size_t off_dq = off_D + up256(rows_pad * 4);
+    const size_t total = off_dq + up256((size_t)B * H * S_q * d * 4);
+    if (total > kFaNoallocScratchBytes) {
+        char msg[160];
+        snprintf(msg, sizeof msg, "this shape needs %zu bytes of scratch, fa_bwd_noalloc has %zu (use fa_bwd)",
+                 total, kFaNoallocScratchBytes);
+        return set_error(FA_ERR_INVALID_ARG, "scratch", msg);
+    }
+    void* base = nullptr;
+    if ((rc = scratch_address(&base)) != FA_OK) return rc;
+    char* b = static_cast<char*>(base);
+    Workspace ws;
+    ws.err = reinterpret_cast<unsigned int*>(b);
+    ws.lse2 = reinterpret_cast<float*>(b + off_lse2);
+    ws.Dws = reinterpret_cast<float*>(b + off_D);
+    ws.dqacc = reinterpret_cast<float*>(b + off_dq);
+    Shape s;
+    s.B = B;
+    s.H = H;
+    s.H_kv = H_kv;
+    s.S_q = S_q;
+    s.S_k = S_k;
+    s.d = d;
+    s.scale = scale;
+    s.causal = causal;
+    s.S_q_pad = S_q_pad;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the preprocess pass also zeroes the dQ accumulator rows this call uses
+    cudaError_t e = launch_preprocess(dtype, dO, O, LSE, ws.Dws, ws.lse2, ws.dqacc, s, S_q_pad, st);
+    if (e != cudaSuccess) return set_error(FA_ERR_CUDA, "preprocess launch", cudaGetErrorString(e));
+    e = dtype != FA_F32 ? launch_bwd_sm103(dtype, Q, K, V, dO, ws, dK, dV, s, st)
+                        : launch_bwd_simt(dtype, Q, K, V, dO, ws, dK, dV, s, st);
+    if (e != cudaSuccess) return set_error(FA_ERR_CUDA, "main kernel launch", cudaGetErrorString(e));
+    e = launch_dq_finalize(dtype, ws.dqacc, dQ, s, st);
+    if (e != cudaSuccess) return set_error(FA_ERR_CUDA, "dq finalize launch", cudaGetErrorString(e));
+    return FA_OK;
+}

@@ -112,6 +112,30 @@ int fa_bwd_host(const void* dO, const void* Q, const void* K, const void* V, con
                 const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv, int S_q,
                 int S_k, int d, float scale, int causal, int dtype, void* stream);
 
+/*
+ * fa_bwd_noalloc -- fa_bwd for callers that cannot allocate device memory
+ * (an allocator or memory pool that owns the GPU's memory, a host that must
+ * not see the implicit synchronization of cudaMalloc / cudaFree, a runtime
+ * that forbids libraries from allocating).  The pages have no counterpart of
+ * this entry point.  Same arguments, layouts and results as fa_bwd; the
+ * caller still passes every input and output buffer, and the library's
+ * scratch comes from one fixed 32 MiB array compiled into the library, which
+ * every GPU that loads the library holds until the process exits.
+ *   * A shape needs 256 + 8*B*H*ceil(S_q/128)*128 + 4*B*H*S_q*d bytes of
+ *     scratch (parts rounded up to 256 bytes); beyond 32 MiB the call returns
+ *     FA_ERR_INVALID_ARG ("scratch: ...") and launches nothing.
+ *   * The first call on a device looks the array's device address up and
+ *     clears its error words: make that first call before any stream capture.
+ *   * Every call shares the array (it keeps the last call's contents; each
+ *     call re-zeroes what must start at zero).  Calls whose GPU work overlaps,
+ *     e.g. on different streams, race: keep them in one stream's order.
+ *   * Bounded-wait timeouts of this variant are not reported by
+ *     fa_check_device.
+ */
+int fa_bwd_noalloc(const void* dO, const void* Q, const void* K, const void* V, const void* O,
+                   const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv,
+                   int S_q, int S_k, int d, float scale, int causal, int dtype, void* stream);
+
 /* Workspace bytes fa_bwd needs for a shape (informational; the library
  * allocates and caches it itself). */
 size_t fa_bwd_workspace_bytes(int B, int H, int S_q, int d);
