@@ -7,7 +7,7 @@
 // (atomicAdd), dK, dV"):
 //   S^T  = K Q^T            P^T  = exp2(S^T * scale*log2e - LSE*log2e)
 //   dP^T = V dO^T           dS^T = P^T * (dP^T - D)
-//   dV  += P^T dO           dK  += dS^T Q        dQacc += dS K  (fp32 atomics)
+//   dV  += P^T dO           dK  += dS^T Q        dQacc += dS K  (fp32 reduction)
 //
 // Design (Blackwell-native, not the pages' one-thread-per-key-row design):
 //   * one CTA owns a 128-row key/value tile of one (batch, kv head) and walks
@@ -16,17 +16,22 @@
 //   * the five per-tile products run on the 5th-generation tensor cores
 //     (tcgen05.mma, M = 128, fp32 accumulation in TMEM).  S^T and dP^T are
 //     computed "key-major" (TMEM lane = key row), so the softmax-gradient
-//     threads own one key row each and write P^T / dS^T back into TMEM as the
-//     A operand of the dV / dK products;
+//     threads own one key row each and write P^T / dS^T back into TMEM, packed
+//     to 16 bits, as the A operand of the dV / dK products;
 //   * TMA (cp.async.bulk.tensor, 128-byte swizzle) stages K, V once and Q, dO
 //     in a multi-stage ring; causal tiles that no query can see are skipped;
-//   * warp roles: warps 0-3 drain the dQ tile from TMEM and add it to the
-//     fp32 accumulator in global memory (red.global.add.v4.f32), warps 4-7
-//     compute P and dS and run the dK / dV epilogue, warp 8 issues TMA,
-//     warp 9 owns TMEM and issues the MMAs;
-//   * two 128-column TMEM buffers alternate roles each iteration: S(i) and
-//     later dQ(i) live in one, dP(i) / dS(i) in the other, so the next S can
-//     be computed while dQ(i) is drained.
+//   * the dQ tile (dS K) is drained from TMEM and added to the fp32
+//     accumulator in global memory: 64 columns with one TMA bulk reduce-add
+//     round staged through the dS shared-memory tile (free once the dQ product
+//     ran), the remaining columns (d = 128) with red.global.add.v4.f32 straight
+//     from registers, which never holds up the next dS tile;
+//   * warp roles: warps 0-3 drain dQ, warps 4-7 compute P and dS and run the
+//     dK / dV epilogue, warp 8 issues TMA, warp 9 owns TMEM and issues MMAs;
+//   * two 128-column TMEM buffers alternate roles each iteration i:
+//       X = buffer[i & 1]:  S(i) -> P(i) (packed, cols 0-63) -> dQ(i)
+//       Y = buffer[~i & 1]: dP(i) -> dS(i) (packed in place, cols 0-63) -> S(i+1)
+//     (Y becomes X of the next iteration); the dQ product is issued first once
+//     dS(i) is ready, so its drain starts as early as possible;
 //   * every mbarrier wait is bounded: on timeout the kernel records an error
 //     word, lets the other roles drop out, waits for its own copies / MMAs in
 //     flight, frees TMEM and returns.
@@ -47,6 +52,7 @@ constexpr int kThreads = 320;
 constexpr int kWarpDrain0 = 0, kWarpSoft0 = 4, kWarpTma = 8, kWarpMma = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 10ull * 1000 * 1000 * 1000;  // 10 s
+constexpr uint32_t kDrainBarrier = 1;                           // named barrier of the drain warps
 
 template <int D>
 struct Cfg {
@@ -56,7 +62,7 @@ struct Cfg {
     static constexpr uint32_t kTileQ_B = BM * D * 2;     // Q or dO tile bytes
     static constexpr uint32_t kBoxK_B = BN * 128;        // one 64-column box of K / V
     static constexpr uint32_t kBoxQ_B = BM * 128;        // one 64-column box of Q / dO
-    static constexpr uint32_t kdS_B = BN * BM * 2;
+    static constexpr uint32_t kdS_B = BN * BM * 2;       // dS tile; also the dQ staging area
     static constexpr uint32_t OFF_K = 0;
     static constexpr uint32_t OFF_V = OFF_K + kTileK_B;
     static constexpr uint32_t OFF_Q = OFF_V + kTileK_B;
@@ -69,23 +75,24 @@ struct Cfg {
     static constexpr uint32_t OFF_MISC = OFF_BAR + kNumBars * 8;
     static constexpr uint32_t SMEM = OFF_MISC + 16;
     static constexpr uint32_t TM_DV = 0, TM_DK = D, TM_BUF0 = 2 * D;
+    static_assert(kdS_B == 2 * BM * 128, "the dS tile doubles as two 128-row x 32-fp32 dQ staging boxes");
 };
 
 // Barrier slots.
 enum {
-    B_KV = 0,
-    B_S_FULL,
-    B_DP_FULL,
-    B_P_READY,
-    B_DS_READY,
-    B_DS_EMPTY,
-    B_DQ_FULL,
-    B_DQ_EMPTY,
-    B_G3,
-    B_G4,
-    B_ACC,
-    B_FINAL,
-    B_STAGE0  // then STAGES "full" barriers, then STAGES "empty" barriers
+    B_KV = 0,      // K, V landed (TMA)
+    B_S_FULL,      // S(i) in TMEM (MMA commit)
+    B_DP_FULL,     // dP(i) in TMEM (MMA commit)
+    B_P_READY,     // P(i) packed in TMEM (4 softmax warps)
+    B_DS_READY,    // dS(i) packed in TMEM and in shared memory (4 softmax warps)
+    B_DS_EMPTY,    // shared dS tile free again: dQ(i) staged out of it and read by TMA (drain)
+    B_DQ_FULL,     // dQ(i) in TMEM (MMA commit)
+    B_DQ_EMPTY,    // dQ(i) copied out of TMEM (4 drain warps)
+    B_G3,          // dV product of iteration i done (MMA commit)
+    B_G4,          // dK product of iteration i done (MMA commit)
+    B_ACC,         // every product done: dK / dV final (MMA commit)
+    B_FINAL,       // MMA shutdown
+    B_STAGE0 = 12  // then STAGES "full" barriers, then STAGES "empty" barriers
 };
 
 struct Params {
@@ -98,7 +105,6 @@ struct Params {
     int B, H, H_kv, S_q, S_k, S_q_pad;
     float scale, scale_log2;
     int causal;
-    int n_kv_tiles;
 };
 
 __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
@@ -108,6 +114,15 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
 __device__ __forceinline__ uint32_t pack2_f16(float lo, float hi) {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+template <bool kBF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    return kBF16 ? pack2_bf16(lo, hi) : pack2_f16(lo, hi);
+}
+template <bool kBF16>
+__device__ __forceinline__ float2 unpack2(uint32_t v) {
+    if (kBF16) return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+    return __half22float2(*reinterpret_cast<__half2*>(&v));
 }
 
 // Bounded wait.  Returns false (and raises the CTA abort flag and the device
@@ -150,21 +165,23 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                     const Params p) {
+                     const __grid_constant__ CUtensorMap tmdQ, const Params p) {
     using C = Cfg<D>;
-    constexpr bool kBF16 = sizeof(T) == 2 && TypeTraits<T>::kId == FA_BF16;
+    constexpr bool kBF16 = TypeTraits<T>::kId == FA_BF16;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = ptx::smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 4);
     auto bar = [&](int i) { return sbase + C::OFF_BAR + 8u * (uint32_t)i; };
     auto bar_full = [&](int s) { return bar(B_STAGE0 + s); };
     auto bar_empty = [&](int s) { return bar(B_STAGE0 + C::STAGES + s); };
 
-    // ---- work assignment: blockIdx.x = key tile (heaviest causal tiles first) x (b, kv head)
+    // ---- work assignment: blockIdx.x = key tile x (b, kv head), so the heaviest causal
+    // key tiles (most query tiles) start first.  Each CTA walks its query tiles from the
+    // last one down, heads innermost: CTAs running side by side reduce into and read the
+    // same dQ / Q / dO tiles at about the same time.
     const int bhkv_count = p.B * p.H_kv;
     const int n_tile = blockIdx.x / bhkv_count;
     const int bkv = blockIdx.x % bhkv_count;
@@ -200,8 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tm_buf0 = tmem + C::TM_BUF0;  // buffer x at tm_buf0 + 128 * x
 
     auto iter_coords = [&](int it, int& bh, int& m0) {
-        const int hh = it / nm;
-        m0 = (m_start + it % nm) * BM;
+        const int hh = it % g;
+        m0 = (m_tiles - 1 - it / g) * BM;
         bh = b * p.H + hk * g + hh;
     };
 
@@ -261,52 +278,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_fence_after();
                 gemm_sd(tm_buf0, sK, sbase + C::OFF_Q);
                 ptx::mma_commit(bar(B_S_FULL));
-                gemm_sd((tm_buf0 + 128), sV, sbase + C::OFF_DO);
+                gemm_sd(tm_buf0 + 128, sV, sbase + C::OFF_DO);
                 ptx::mma_commit(bar(B_DP_FULL));
             }
             for (int it = 0; ok && it < n_it; ++it) {
                 const int s = it % C::STAGES;
-                const int bs = it & 1;
+                const uint32_t X = tm_buf0 + 128 * (it & 1);        // S -> P -> dQ of this iteration
+                const uint32_t Y = tm_buf0 + 128 * ((it & 1) ^ 1);  // dP -> dS of this iteration, S of the next
                 const uint32_t sQ = sbase + C::OFF_Q + s * C::kTileQ_B;
                 const uint32_t sdO = sbase + C::OFF_DO + s * C::kTileQ_B;
-                // dV += P^T dO   (A = P^T in TMEM, 16 query columns = 8 packed columns per step)
+                // dV += P^T dO   (A = P^T in TMEM X[0,64): 16 query columns = 8 packed columns per step)
                 if (!(ok = wait_bar(bar(B_P_READY), it & 1, abort_flag, p.err))) break;
                 ptx::tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < BM / 16; ++k)
-                    ptx::mma_ts(tmem + C::TM_DV, (tm_buf0 + 128 * bs) + k * 8,
-                                ptx::sw128_desc(sdO + k * 2048, C::kBoxQ_B, 1024), ID_KV,
-                                (it > 0 || k > 0) ? 1u : 0u);
+                    ptx::mma_ts(tmem + C::TM_DV, X + k * 8, ptx::sw128_desc(sdO + k * 2048, C::kBoxQ_B, 1024),
+                                ID_KV, (it > 0 || k > 0) ? 1u : 0u);
                 ptx::mma_commit(bar(B_G3));
-                // dK += dS^T Q
+                // dQ = dS K first (its drain is the longest chain), into X once the dV
+                // product stopped reading P from it
                 if (!(ok = wait_bar(bar(B_DS_READY), it & 1, abort_flag, p.err))) break;
-                ptx::tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < BM / 16; ++k)
-                    ptx::mma_ts(tmem + C::TM_DK, (tm_buf0 + 128 * (bs ^ 1)) + k * 8,
-                                ptx::sw128_desc(sQ + k * 2048, C::kBoxQ_B, 1024), ID_KV,
-                                (it > 0 || k > 0) ? 1u : 0u);
-                ptx::mma_commit(bar(B_G4));
-                // dQ = dS K into the S buffer once the dV product stopped reading P from it
                 if (!(ok = wait_bar(bar(B_G3), it & 1, abort_flag, p.err))) break;
                 ptx::tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k)
-                    ptx::mma_ss((tm_buf0 + 128 * bs), ptx::sw128_desc(sdS + k * 2048, BN * 128, 1024),
+                    ptx::mma_ss(X, ptx::sw128_desc(sdS + k * 2048, BN * 128, 1024),
                                 ptx::sw128_desc(sK + k * 2048, C::kBoxK_B, 1024), ID_Q, k > 0);
                 ptx::mma_commit(bar(B_DQ_FULL));
-                ptx::mma_commit(bar_empty(s));
-                ptx::mma_commit(bar(B_DS_EMPTY));
+                // dK += dS^T Q   (A = dS^T in TMEM Y[0,64))
+#pragma unroll
+                for (int k = 0; k < BM / 16; ++k)
+                    ptx::mma_ts(tmem + C::TM_DK, Y + k * 8, ptx::sw128_desc(sQ + k * 2048, C::kBoxQ_B, 1024),
+                                ID_KV, (it > 0 || k > 0) ? 1u : 0u);
+                ptx::mma_commit(bar(B_G4));
+                ptx::mma_commit(bar_empty(s));  // Q(i), dO(i) no longer read
                 if (it + 1 < n_it) {
+                    // S(i+1) into Y once the dK product stopped reading dS(i) from it
                     const int s1 = (it + 1) % C::STAGES;
                     if (!(ok = wait_bar(bar_full(s1), ((it + 1) / C::STAGES) & 1, abort_flag, p.err))) break;
                     if (!(ok = wait_bar(bar(B_G4), it & 1, abort_flag, p.err))) break;
                     ptx::tc_fence_after();
-                    gemm_sd((tm_buf0 + 128 * (bs ^ 1)), sK, sbase + C::OFF_Q + s1 * C::kTileQ_B);
+                    gemm_sd(Y, sK, sbase + C::OFF_Q + s1 * C::kTileQ_B);
                     ptx::mma_commit(bar(B_S_FULL));
+                    // dP(i+1) into X once dQ(i) left it
                     if (!(ok = wait_bar(bar(B_DQ_EMPTY), it & 1, abort_flag, p.err))) break;
                     ptx::tc_fence_after();
-                    gemm_sd((tm_buf0 + 128 * bs), sV, sbase + C::OFF_DO + s1 * C::kTileQ_B);
+                    gemm_sd(X, sV, sbase + C::OFF_DO + s1 * C::kTileQ_B);
                     ptx::mma_commit(bar(B_DP_FULL));
                 }
             }
@@ -322,72 +339,93 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const int j = n0 + t;
         const bool row_valid = j < p.S_k;
+        uint8_t* sdS_row = smem + C::OFF_DS + (t >> 3) * 1024 + (t & 7) * 128;
         bool ok = !*abort_flag;
         for (int it = 0; ok && it < n_it; ++it) {
             const int s = it % C::STAGES;
-            const int bs = it & 1;
+            const uint32_t X = tm_buf0 + 128 * (it & 1) + lane_off;
+            const uint32_t Y = tm_buf0 + 128 * ((it & 1) ^ 1) + lane_off;
             int bh, m0;
             iter_coords(it, bh, m0);
-            const bool mask_tile = !row_valid ? true : (p.causal && (n0 + BN - 1 > m0 + off));
+            // warp-uniform: the chosen loop holds .sync.aligned TMEM accesses; the
+            // per-element selects inside the masked loop handle each lane's own row
+            const bool mask_tile =
+                __any_sync(0xffffffffu, !row_valid || (p.causal && (n0 + BN - 1 > m0 + off)));
             const float* sl = reinterpret_cast<const float*>(smem + C::OFF_LSE + s * BM * 4);
             const float* sd = reinterpret_cast<const float*>(smem + C::OFF_DD + s * BM * 4);
             if (!(ok = wait_bar_warp(bar_full(s), (it / C::STAGES) & 1, abort_flag, p.err))) break;
             if (!(ok = wait_bar_warp(bar(B_S_FULL), it & 1, abort_flag, p.err))) break;
             ptx::tc_fence_after();
-            float P[BM];
-#pragma unroll
-            for (int c = 0; c < BM / 32; ++c) {
-                uint32_t r[32];
-                ptx::tmem_ld32((tm_buf0 + 128 * bs) + lane_off + c * 32, r);
+            // P = exp2(S * scale*log2e - LSE*log2e), packed to 16 bits in place (X[0,64)).
+            // Masking is decided once per tile, outside the unrolled loop, so the 64
+            // independent exp chains of a chunk stay one basic block.
+            uint32_t Pp[BM / 2];
+            auto p_chunk = [&](int c, bool masked) {
+                uint32_t r[64];
+                ptx::tmem_ld32p(X + c * 64, r);
+                ptx::tmem_ld32p(X + c * 64 + 32, r + 32);
                 ptx::tmem_wait_ld();
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const int q = c * 32 + k;
-                    float x = ptx::ex2(fmaf(__uint_as_float(r[k]), p.scale_log2, -sl[q]));
-                    if (mask_tile) {
-                        const bool vis = row_valid && (!p.causal || j <= m0 + q + off);
-                        x = vis ? x : 0.f;
+                for (int k = 0; k < 64; k += 4) {
+                    const int q = c * 64 + k;
+                    const float4 l4 = *reinterpret_cast<const float4*>(sl + q);
+                    float x0 = ptx::ex2(fmaf(__uint_as_float(r[k + 0]), p.scale_log2, -l4.x));
+                    float x1 = ptx::ex2(fmaf(__uint_as_float(r[k + 1]), p.scale_log2, -l4.y));
+                    float x2 = ptx::ex2(fmaf(__uint_as_float(r[k + 2]), p.scale_log2, -l4.z));
+                    float x3 = ptx::ex2(fmaf(__uint_as_float(r[k + 3]), p.scale_log2, -l4.w));
+                    if (masked) {
+                        const int lim = m0 + q + off;  // key j visible to query m0+q+u iff j <= lim+u
+                        x0 = (row_valid && (!p.causal || j <= lim + 0)) ? x0 : 0.f;
+                        x1 = (row_valid && (!p.causal || j <= lim + 1)) ? x1 : 0.f;
+                        x2 = (row_valid && (!p.causal || j <= lim + 2)) ? x2 : 0.f;
+                        x3 = (row_valid && (!p.causal || j <= lim + 3)) ? x3 : 0.f;
                     }
-                    P[q] = x;
+                    Pp[q / 2] = pack2<kBF16>(x0, x1);
+                    Pp[q / 2 + 1] = pack2<kBF16>(x2, x3);
                 }
-                uint32_t pk[16];
+                ptx::tmem_st32(X + c * 32, Pp + c * 32);
+            };
+            if (mask_tile) {
 #pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    pk[k] = kBF16 ? pack2_bf16(P[c * 32 + 2 * k], P[c * 32 + 2 * k + 1])
-                                  : pack2_f16(P[c * 32 + 2 * k], P[c * 32 + 2 * k + 1]);
-                ptx::tmem_st16((tm_buf0 + 128 * bs) + lane_off + c * 16, pk);
+                for (int c = 0; c < BM / 64; ++c) p_chunk(c, true);
+            } else {
+#pragma unroll
+                for (int c = 0; c < BM / 64; ++c) p_chunk(c, false);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(B_P_READY));
 
+            // dS = P * (dP - D): packed in place into Y[0,64) for the dK product and
+            // into the shared dS tile (key-major rows, 128-byte swizzled MN-major) for dQ.
             if (!(ok = wait_bar_warp(bar(B_DP_FULL), it & 1, abort_flag, p.err))) break;
             if (it > 0 && !(ok = wait_bar_warp(bar(B_DS_EMPTY), (it - 1) & 1, abort_flag, p.err))) break;
             ptx::tc_fence_after();
-            uint8_t* sdS_row = smem + C::OFF_DS + (t >> 3) * 1024 + (t & 7) * 128;
 #pragma unroll
             for (int c = 0; c < BM / 32; ++c) {
                 uint32_t r[32];
-                ptx::tmem_ld32((tm_buf0 + 128 * (bs ^ 1)) + lane_off + c * 32, r);
+                ptx::tmem_ld32p(Y + c * 32, r);
                 ptx::tmem_wait_ld();
                 uint32_t pk[16];
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int q = c * 32 + 2 * k;
-                    const float d0 = P[q] * (__uint_as_float(r[2 * k]) - sd[q]);
-                    const float d1 = P[q + 1] * (__uint_as_float(r[2 * k + 1]) - sd[q + 1]);
-                    pk[k] = kBF16 ? pack2_bf16(d0, d1) : pack2_f16(d0, d1);
+                for (int k = 0; k < 32; k += 4) {
+                    const int q = c * 32 + k;
+                    const float4 d4 = *reinterpret_cast<const float4*>(sd + q);
+                    const float2 p01 = unpack2<kBF16>(Pp[q / 2]);
+                    const float2 p23 = unpack2<kBF16>(Pp[q / 2 + 1]);
+                    pk[k / 2] = pack2<kBF16>(p01.x * (__uint_as_float(r[k]) - d4.x),
+                                             p01.y * (__uint_as_float(r[k + 1]) - d4.y));
+                    pk[k / 2 + 1] = pack2<kBF16>(p23.x * (__uint_as_float(r[k + 2]) - d4.z),
+                                                 p23.y * (__uint_as_float(r[k + 3]) - d4.w));
                 }
-                ptx::tmem_st16((tm_buf0 + 128 * (bs ^ 1)) + lane_off + c * 16, pk);
-                // dS (key-major rows, query-contiguous) for the dQ product:
-                // 128-byte swizzled MN-major layout, 8-query chunks.
+                ptx::tmem_st16(Y + c * 16, pk);  // columns already read
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int q0 = c * 32 + u * 8;
                     const int blk = q0 >> 6, chunk = (q0 & 63) >> 3;
-                    uint4 v = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-                    *reinterpret_cast<uint4*>(sdS_row + blk * (BN * 128) + ((chunk ^ (t & 7)) << 4)) = v;
+                    *reinterpret_cast<uint4*>(sdS_row + blk * (BN * 128) + ((chunk ^ (t & 7)) << 4)) =
+                        make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
                 }
             }
             ptx::tmem_wait_st();
@@ -406,8 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t rv[32], rk[32];
                 if (n_it > 0) {
-                    ptx::tmem_ld32(tmem + C::TM_DV + lane_off + c * 32, rv);
-                    ptx::tmem_ld32(tmem + C::TM_DK + lane_off + c * 32, rk);
+                    ptx::tmem_ld32p(tmem + C::TM_DV + lane_off + c * 32, rv);
+                    ptx::tmem_ld32p(tmem + C::TM_DK + lane_off + c * 32, rk);
                     ptx::tmem_wait_ld();
                 } else {
 #pragma unroll
@@ -419,10 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int e = u * 8 + 2 * k;
-                        const float v0 = __uint_as_float(rv[e]), v1 = __uint_as_float(rv[e + 1]);
-                        const float k0 = __uint_as_float(rk[e]) * p.scale, k1 = __uint_as_float(rk[e + 1]) * p.scale;
-                        ov[k] = kBF16 ? pack2_bf16(v0, v1) : pack2_f16(v0, v1);
-                        ok4[k] = kBF16 ? pack2_bf16(k0, k1) : pack2_f16(k0, k1);
+                        ov[k] = pack2<kBF16>(__uint_as_float(rv[e]), __uint_as_float(rv[e + 1]));
+                        ok4[k] = pack2<kBF16>(__uint_as_float(rk[e]) * p.scale, __uint_as_float(rk[e + 1]) * p.scale);
                     }
                     if (row_valid) {
                         *reinterpret_cast<uint4*>(dVrow + c * 32 + u * 8) = make_uint4(ov[0], ov[1], ov[2], ov[3]);
@@ -433,33 +469,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= kWarpDrain0 && warp < kWarpDrain0 + 4) {
         // ------------------------------------------------------------ dQ drain (one query row per thread)
+        // dQ(i) rows -> registers; columns [0, 64) -> shared dS tile (two 128 x 32 fp32
+        // boxes, 128-byte swizzle) -> one TMA reduce-add round; columns [64, d) ->
+        // red.global.add.v4.f32.  The dS tile is released (B_DS_EMPTY) as soon as the
+        // bulk reduce has read it.
         const int t = (warp - kWarpDrain0) * 32 + lane;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const bool issuer = t == 0;
+        uint8_t* stage_row = smem + C::OFF_DS + t * 128;
         bool ok = !*abort_flag;
         for (int it = 0; ok && it < n_it; ++it) {
-            const int bs = it & 1;
+            const uint32_t X = tm_buf0 + 128 * (it & 1) + lane_off;
             int bh, m0;
             iter_coords(it, bh, m0);
-            if (!(ok = wait_bar_warp(bar(B_DQ_FULL), it & 1, abort_flag, p.err))) break;
+            // all four drain warps take the same decision: they share a named barrier below
+            ok = ptx::named_bar_and(kDrainBarrier, 128, wait_bar(bar(B_DQ_FULL), it & 1, abort_flag, p.err));
+            if (!ok) break;
             ptx::tc_fence_after();
-            uint32_t r[D / 32][32];
+            uint32_t r[D];
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32((tm_buf0 + 128 * bs) + lane_off + c * 32, r[c]);
+            for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32p(X + c * 32, r + c * 32);
             ptx::tmem_wait_ld();
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(B_DQ_EMPTY));
-            const int row = m0 + t;
-            if (row < p.S_q) {
-                float* dst = p.dqacc + ((size_t)bh * p.S_q + row) * D;
+            // The dS tile is free: the dQ product that read it is complete (B_DQ_FULL), and
+            // the previous bulk reduce finished reading it before B_DS_EMPTY let the next dS in.
 #pragma unroll
-                for (int c = 0; c < D / 4; ++c)
-                    ptx::red_add_v4(dst + 4 * c, __uint_as_float(r[c / 8][(4 * c) % 32]),
-                                    __uint_as_float(r[c / 8][(4 * c + 1) % 32]),
-                                    __uint_as_float(r[c / 8][(4 * c + 2) % 32]),
-                                    __uint_as_float(r[c / 8][(4 * c + 3) % 32]));
+            for (int bx = 0; bx < 2; ++bx)
+#pragma unroll
+                for (int cq = 0; cq < 8; ++cq) {
+                    const int e = bx * 32 + cq * 4;
+                    *reinterpret_cast<uint4*>(stage_row + bx * (BM * 128) + ((cq ^ (t & 7)) << 4)) =
+                        make_uint4(r[e], r[e + 1], r[e + 2], r[e + 3]);
+                }
+            ptx::fence_proxy_async_smem();
+            ptx::named_bar_sync(kDrainBarrier, 128);
+            if (issuer) {
+                ptx::tma_reduce_add_3d(&tmdQ, sbase + C::OFF_DS, 0, m0, bh);
+                ptx::tma_reduce_add_3d(&tmdQ, sbase + C::OFF_DS + BM * 128, 32, m0, bh);
+                ptx::bulk_commit_group();
+                ptx::bulk_wait_read_all();
+                ptx::mbar_arrive(bar(B_DS_EMPTY));
+            }
+            if (D > 64) {
+                const int row = m0 + t;
+                if (row < p.S_q) {
+                    float* dst = p.dqacc + ((size_t)bh * p.S_q + row) * D;
+#pragma unroll
+                    for (int c = 16; c < D / 4; ++c)
+                        ptx::red_add_v4(dst + 4 * c, __uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]),
+                                        __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
+                }
             }
         }
+        if (issuer) ptx::bulk_wait_all();
     }
 
     ptx::tc_fence_before();
@@ -489,19 +553,19 @@ EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-// 3-D view [heads][rows][D] of a [B, heads, rows, D] tensor, box = 64 columns x 128 rows.
-bool make_map(CUtensorMap* m, const void* base, int dtype, int heads, int rows, int D) {
+// 3-D view [heads][rows][D] of a [B, heads, rows, D] tensor with a 128-byte-wide,
+// 128-row box (64 16-bit or 32 fp32 columns) and 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, int heads, int rows,
+              int D) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)heads};
-    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)rows * D * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * esize, (cuuint64_t)rows * D * esize};
+    const cuuint32_t box[3] = {(cuuint32_t)(128 / esize), 128, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
-    const CUtensorMapDataType dt =
-        dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <typename T, int D>
@@ -509,10 +573,12 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, const void* dO
                      const Workspace& ws, void* dK, void* dV, const Shape& s, cudaStream_t st) {
     using C = Cfg<D>;
     static_assert(C::SMEM <= 232448, "shared memory budget");
-    CUtensorMap tq, tk, tv, tdo;
-    const int dt = TypeTraits<T>::kId;
-    if (!make_map(&tq, Q, dt, s.B * s.H, s.S_q, D) || !make_map(&tk, K, dt, s.B * s.H_kv, s.S_k, D) ||
-        !make_map(&tv, V, dt, s.B * s.H_kv, s.S_k, D) || !make_map(&tdo, dO, dt, s.B * s.H, s.S_q, D))
+    CUtensorMap tq, tk, tv, tdo, tdq;
+    const CUtensorMapDataType dt =
+        TypeTraits<T>::kId == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (!make_map(&tq, Q, dt, 2, s.B * s.H, s.S_q, D) || !make_map(&tk, K, dt, 2, s.B * s.H_kv, s.S_k, D) ||
+        !make_map(&tv, V, dt, 2, s.B * s.H_kv, s.S_k, D) || !make_map(&tdo, dO, dt, 2, s.B * s.H, s.S_q, D) ||
+        !make_map(&tdq, ws.dqacc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s.B * s.H, s.S_q, D))
         return cudaErrorInvalidValue;
     Params p;
     p.lse2 = ws.lse2;
@@ -530,12 +596,11 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, const void* dO
     p.scale = s.scale;
     p.scale_log2 = s.scale * 1.4426950408889634f;
     p.causal = s.causal;
-    p.n_kv_tiles = (s.S_k + BN - 1) / BN;
     auto kern = bwd_sm103_kernel<T, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
-    const long grid = (long)p.n_kv_tiles * s.B * s.H_kv;
-    kern<<<(unsigned)grid, kThreads, C::SMEM, st>>>(tq, tk, tv, tdo, p);
+    const long grid = (long)((s.S_k + BN - 1) / BN) * s.B * s.H_kv;
+    kern<<<(unsigned)grid, kThreads, C::SMEM, st>>>(tq, tk, tv, tdo, tdq, p);
     return cudaGetLastError();
 }
 

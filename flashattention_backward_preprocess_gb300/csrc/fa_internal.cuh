@@ -8,7 +8,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/fa.h"
+#include "fa.h"  // include/fa.h (nvcc -I include)
 
 namespace fa {
 
