@@ -21,10 +21,9 @@
 //   * TMA (cp.async.bulk.tensor, 128-byte swizzle) stages K, V once and Q, dO
 //     in a multi-stage ring; causal tiles that no query can see are skipped;
 //   * the dQ tile (dS K) is drained from TMEM and added to the fp32
-//     accumulator in global memory: 64 columns with one TMA bulk reduce-add
-//     round staged through the dS shared-memory tile (free once the dQ product
-//     ran), the remaining columns (d = 128) with red.global.add.v4.f32 straight
-//     from registers, which never holds up the next dS tile;
+//     accumulator in global memory with TMA bulk reduce-adds, 64 columns per
+//     round, staged through the dS shared-memory tile (free once the dQ product
+//     ran);
 //   * warp roles: warps 0-3 drain dQ, warps 4-7 compute P and dS and run the
 //     dK / dV epilogue, warp 8 issues TMA, warp 9 owns TMEM and issues MMAs;
 //   * two 128-column TMEM buffers alternate roles each iteration i:
@@ -98,7 +97,6 @@ enum {
 struct Params {
     const float* lse2;
     const float* Dws;
-    float* dqacc;
     void* dK;
     void* dV;
     unsigned int* err;
@@ -469,10 +467,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= kWarpDrain0 && warp < kWarpDrain0 + 4) {
         // ------------------------------------------------------------ dQ drain (one query row per thread)
-        // dQ(i) rows -> registers; columns [0, 64) -> shared dS tile (two 128 x 32 fp32
-        // boxes, 128-byte swizzle) -> one TMA reduce-add round; columns [64, d) ->
-        // red.global.add.v4.f32.  The dS tile is released (B_DS_EMPTY) as soon as the
-        // bulk reduce has read it.
+        // dQ(i) rows -> registers -> shared dS tile (two 128 x 32 fp32 boxes, 128-byte
+        // swizzle) -> TMA reduce-add into the fp32 accumulator, 64 columns per round.
+        // Only bulk reductions are used: per-thread red.global instructions would
+        // crowd the SM's memory-instruction path the MMA warp issues through.  The dS
+        // tile is released (B_DS_EMPTY) once the last bulk reduce has read it.
         const int t = (warp - kWarpDrain0) * 32 + lane;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const bool issuer = t == 0;
@@ -496,31 +495,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             // The dS tile is free: the dQ product that read it is complete (B_DQ_FULL), and
             // the previous bulk reduce finished reading it before B_DS_EMPTY let the next dS in.
 #pragma unroll
-            for (int bx = 0; bx < 2; ++bx)
-#pragma unroll
-                for (int cq = 0; cq < 8; ++cq) {
-                    const int e = bx * 32 + cq * 4;
-                    *reinterpret_cast<uint4*>(stage_row + bx * (BM * 128) + ((cq ^ (t & 7)) << 4)) =
-                        make_uint4(r[e], r[e + 1], r[e + 2], r[e + 3]);
+            for (int h = 0; h < D / 64; ++h) {
+                if (h > 0) {  // the staging area is free once the previous round was read
+                    if (issuer) ptx::bulk_wait_read_all();
+                    ptx::named_bar_sync(kDrainBarrier, 128);
                 }
-            ptx::fence_proxy_async_smem();
-            ptx::named_bar_sync(kDrainBarrier, 128);
+#pragma unroll
+                for (int bx = 0; bx < 2; ++bx)
+#pragma unroll
+                    for (int cq = 0; cq < 8; ++cq) {
+                        const int e = h * 64 + bx * 32 + cq * 4;
+                        *reinterpret_cast<uint4*>(stage_row + bx * (BM * 128) + ((cq ^ (t & 7)) << 4)) =
+                            make_uint4(r[e], r[e + 1], r[e + 2], r[e + 3]);
+                    }
+                ptx::fence_proxy_async_smem();
+                ptx::named_bar_sync(kDrainBarrier, 128);
+                if (issuer) {
+                    ptx::tma_reduce_add_3d(&tmdQ, sbase + C::OFF_DS, h * 64, m0, bh);
+                    ptx::tma_reduce_add_3d(&tmdQ, sbase + C::OFF_DS + BM * 128, h * 64 + 32, m0, bh);
+                    ptx::bulk_commit_group();
+                }
+            }
             if (issuer) {
-                ptx::tma_reduce_add_3d(&tmdQ, sbase + C::OFF_DS, 0, m0, bh);
-                ptx::tma_reduce_add_3d(&tmdQ, sbase + C::OFF_DS + BM * 128, 32, m0, bh);
-                ptx::bulk_commit_group();
                 ptx::bulk_wait_read_all();
                 ptx::mbar_arrive(bar(B_DS_EMPTY));
-            }
-            if (D > 64) {
-                const int row = m0 + t;
-                if (row < p.S_q) {
-                    float* dst = p.dqacc + ((size_t)bh * p.S_q + row) * D;
-#pragma unroll
-                    for (int c = 16; c < D / 4; ++c)
-                        ptx::red_add_v4(dst + 4 * c, __uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]),
-                                        __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
-                }
             }
         }
         if (issuer) ptx::bulk_wait_all();
@@ -583,7 +581,6 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, const void* dO
     Params p;
     p.lse2 = ws.lse2;
     p.Dws = ws.Dws;
-    p.dqacc = ws.dqacc;
     p.dK = dK;
     p.dV = dV;
     p.err = ws.err;
