@@ -199,8 +199,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         if ((sbase & 1023u) != 0) atomicOr(p.err, kErrSmemAlign);
         *abort_flag = (sbase & 1023u) != 0;
-        for (int i = 0; i < (int)C::kNumBars; ++i)
-            ptx::mbar_init(bar(i), (i == B_P_READY || i == B_DS_READY || i == B_DQ_EMPTY) ? 4u : 1u);
+        for (int i = 0; i < (int)C::kNumBars; ++i) {
+            uint32_t count = (i == B_P_READY || i == B_DS_READY || i == B_DQ_EMPTY) ? 4u : 1u;
+            if (D == 128 && i >= B_STAGE0 + C::STAGES) count = 2;  // stage "empty": MMA + drain
+            ptx::mbar_init(bar(i), count);
+        }
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
     }
@@ -309,7 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mma_ts(tmem + C::TM_DK, Y + k * 8, ptx::sw128_desc(sQ + k * 2048, C::kBoxQ_B, 1024),
                                 ID_KV, (it > 0 || k > 0) ? 1u : 0u);
                 ptx::mma_commit(bar(B_G4));
-                ptx::mma_commit(bar_empty(s));  // Q(i), dO(i) no longer read
+                // Q(i), dO(i) no longer read by MMAs (for d = 128 the stage is free only once
+                // the drain also arrived: it stages half of dQ(i) in the dO tile)
+                ptx::mma_commit(bar_empty(s));
                 if (it + 1 < n_it) {
                     // S(i+1) into Y once the dK product stopped reading dS(i) from it
                     const int s1 = (it + 1) % C::STAGES;
@@ -467,17 +472,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= kWarpDrain0 && warp < kWarpDrain0 + 4) {
         // ------------------------------------------------------------ dQ drain (one query row per thread)
-        // dQ(i) rows -> registers -> shared dS tile (two 128 x 32 fp32 boxes, 128-byte
-        // swizzle) -> TMA reduce-add into the fp32 accumulator, 64 columns per round.
-        // Only bulk reductions are used: per-thread red.global instructions would
-        // crowd the SM's memory-instruction path the MMA warp issues through.  The dS
-        // tile is released (B_DS_EMPTY) once the last bulk reduce has read it.
+        // dQ(i) rows -> registers -> shared memory as 128 x 32 fp32 boxes (128-byte
+        // swizzle) -> TMA reduce-add into the fp32 accumulator.  Columns [0, 64) are
+        // staged in the dS tile (free once the dQ product ran), columns [64, 128) in
+        // the dO tile of the same iteration (free once the dV product ran), so both
+        // bulk reductions are in flight together.  Only bulk reductions are used:
+        // per-thread red.global instructions would crowd the SM's memory-instruction
+        // path the MMA warp issues through.  The dS tile is released (B_DS_EMPTY) once
+        // its bulk reduce has read it; the Q / dO stage (d = 128) needs two arrivals,
+        // this drain's once the other bulk reduce has read it and the MMA warp's once
+        // the dK product (which reads Q) is done.
         const int t = (warp - kWarpDrain0) * 32 + lane;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const bool issuer = t == 0;
-        uint8_t* stage_row = smem + C::OFF_DS + t * 128;
         bool ok = !*abort_flag;
         for (int it = 0; ok && it < n_it; ++it) {
+            const int s = it % C::STAGES;
             const uint32_t X = tm_buf0 + 128 * (it & 1) + lane_off;
             int bh, m0;
             iter_coords(it, bh, m0);
@@ -492,33 +502,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(B_DQ_EMPTY));
-            // The dS tile is free: the dQ product that read it is complete (B_DQ_FULL), and
-            // the previous bulk reduce finished reading it before B_DS_EMPTY let the next dS in.
+            // Both staging areas are free: the dQ product (reads dS) and, before it, the dV
+            // product (reads dO) are complete (B_DQ_FULL); the previous bulk reduce out of the
+            // dS tile was read before B_DS_EMPTY let the next dS in.
 #pragma unroll
             for (int h = 0; h < D / 64; ++h) {
-                if (h > 0) {  // the staging area is free once the previous round was read
-                    if (issuer) ptx::bulk_wait_read_all();
-                    ptx::named_bar_sync(kDrainBarrier, 128);
-                }
+                uint8_t* area = smem + (h == 0 ? C::OFF_DS : C::OFF_DO + s * C::kTileQ_B);
 #pragma unroll
                 for (int bx = 0; bx < 2; ++bx)
 #pragma unroll
                     for (int cq = 0; cq < 8; ++cq) {
                         const int e = h * 64 + bx * 32 + cq * 4;
-                        *reinterpret_cast<uint4*>(stage_row + bx * (BM * 128) + ((cq ^ (t & 7)) << 4)) =
+                        *reinterpret_cast<uint4*>(area + bx * (BM * 128) + t * 128 + ((cq ^ (t & 7)) << 4)) =
                             make_uint4(r[e], r[e + 1], r[e + 2], r[e + 3]);
                     }
-                ptx::fence_proxy_async_smem();
-                ptx::named_bar_sync(kDrainBarrier, 128);
-                if (issuer) {
-                    ptx::tma_reduce_add_3d(&tmdQ, sbase + C::OFF_DS, h * 64, m0, bh);
-                    ptx::tma_reduce_add_3d(&tmdQ, sbase + C::OFF_DS + BM * 128, h * 64 + 32, m0, bh);
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::named_bar_sync(kDrainBarrier, 128);
+            if (issuer) {
+#pragma unroll
+                for (int h = 0; h < D / 64; ++h) {  // one bulk group per staging area, dS tile first
+                    const uint32_t area = sbase + (h == 0 ? C::OFF_DS : C::OFF_DO + s * C::kTileQ_B);
+                    ptx::tma_reduce_add_3d(&tmdQ, area, h * 64, m0, bh);
+                    ptx::tma_reduce_add_3d(&tmdQ, area + BM * 128, h * 64 + 32, m0, bh);
                     ptx::bulk_commit_group();
                 }
-            }
-            if (issuer) {
-                ptx::bulk_wait_read_all();
-                ptx::mbar_arrive(bar(B_DS_EMPTY));
+                if (D == 128) {
+                    ptx::bulk_wait_read_1();  // the dS-tile group (the older one) was read
+                    ptx::mbar_arrive(bar(B_DS_EMPTY));
+                    ptx::bulk_wait_read_all();
+                    ptx::mbar_arrive(bar_empty(s));  // second of two arrivals (MMA commit after dK)
+                } else {
+                    ptx::bulk_wait_read_all();
+                    ptx::mbar_arrive(bar(B_DS_EMPTY));
+                }
             }
         }
         if (issuer) ptx::bulk_wait_all();
