@@ -147,7 +147,7 @@ def kernel_source_hash() -> str:
     """Hash of the main kernel's sources: ncu traffic counters are only valid for this exact kernel."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("bwd_sm103.cu", "sm103_ptx.cuh", "fa_internal.cuh"):
+    for f in ("bwd_sm103.cu", "sm103_ptx.cuh", "bounded_wait.cuh", "fa_internal.cuh"):
         with open(os.path.join(ROOT, "flashattention_backward_preprocess_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -198,6 +198,8 @@ def run_reference(args, world, rank):
     w = WORKLOADS[BENCH_WORKLOAD]
     sample_b = 1
     ws = w.with_(B=sample_b)
+    if args.ref_seq:  # a shorter sample of the same heads and head dim (quick checks)
+        ws = ws.with_(S_q=min(args.ref_seq, w.S_q), S_k=min(args.ref_seq, w.S_k))
     Q, K, V, dO = make_inputs(ws)
     args64 = [x.to(torch.float64).numpy() for x in (Q, K, V, dO)]
     O, LSE = oracle.ref_fwd(args64[0], args64[1], args64[2], w.scale, w.causal)
@@ -214,7 +216,7 @@ def run_reference(args, world, rank):
     ms = 1e3 * statistics.mean(times)
     value = ws.flops() / (ms / 1e3) / 1e12
     sample = (f"each step: fp64 oracle ref_bwd on batch entry 0 of {w.B} (all {w.H} heads, "
-              f"S={w.S_q}, d={w.d}, causal), {ws.flops():.3g} flops")
+              f"S={ws.S_q}, d={w.d}, causal), {ws.flops():.3g} flops")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -237,6 +239,8 @@ def main():
     ap.add_argument("--cpu-batches", type=int, default=2,
                     help="batch entries of the workload the CPU oracle baseline runs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seq", type=int, default=0,
+                    help="reference arm: limit the sampled sequence length (0 = the workload's)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

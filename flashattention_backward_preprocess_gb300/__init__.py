@@ -23,6 +23,7 @@ from .binding import (  # noqa: F401
     fa_last_error,
     fa_profile,
     fa_profile_read,
+    fa_selftest_timeout,
     fa_shutdown,
     fa_version,
     library_path,

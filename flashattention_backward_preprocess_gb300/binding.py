@@ -28,8 +28,8 @@ _lib = None
 
 #: every symbol include/fa.h declares
 EXPORTS = ("fa_bwd", "fa_bwd_noalloc", "fa_bwd_preprocess", "fa_fwd", "fa_bwd_host", "fa_bwd_workspace_bytes",
-           "fa_check_device", "fa_profile", "fa_profile_read", "fa_last_error", "fa_shutdown",
-           "fa_version")
+           "fa_check_device", "fa_profile", "fa_profile_read", "fa_selftest_timeout",
+           "fa_last_error", "fa_shutdown", "fa_version")
 
 
 class FaError(RuntimeError):
@@ -72,6 +72,8 @@ def load_library(path: str | None = None):
         lib.fa_profile.restype = I
         lib.fa_profile_read.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]
         lib.fa_profile_read.restype = I
+        lib.fa_selftest_timeout.argtypes = [ctypes.c_ulonglong, V]
+        lib.fa_selftest_timeout.restype = I
         lib.fa_last_error.restype = ctypes.c_char_p
         lib.fa_version.restype = ctypes.c_char_p
         lib.fa_shutdown.restype = None
@@ -242,6 +244,11 @@ def fa_profile_read():
     n = ctypes.c_int()
     _check(load_library().fa_profile_read(ms, ctypes.byref(n)))
     return float(ms[0]), float(ms[1]), float(ms[2]), int(n.value)
+
+
+def fa_selftest_timeout(limit_ns: int = 1_000_000, stream=None) -> None:
+    """Launch the bounded-wait self-test (a wait that must run out after limit_ns)."""
+    _check(load_library().fa_selftest_timeout(int(limit_ns), _stream(stream)))
 
 
 def fa_check_device(stream=None) -> None:

@@ -426,6 +426,19 @@ int fa_profile_read(float* ms, int* calls) {
     return FA_OK;
 }
 
+int fa_selftest_timeout(unsigned long long limit_ns, void* stream) {
+    g_last_error.clear();
+    if (limit_ns == 0 || limit_ns > 1000000000ull)
+        return fail(FA_ERR_INVALID_ARG, "limit_ns", "must be in (0, 1e9] nanoseconds");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void* base = nullptr;
+    int rc = get_workspace(st, 256, &base);
+    if (rc != FA_OK) return rc;
+    cudaError_t e = launch_wait_selftest(static_cast<unsigned int*>(base), limit_ns, st);
+    if (e != cudaSuccess) return cuda_fail("self-test launch", e);
+    return FA_OK;
+}
+
 const char* fa_last_error(void) { return g_last_error.c_str(); }
 
 void fa_shutdown(void) {

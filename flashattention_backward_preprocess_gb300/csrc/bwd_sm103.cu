@@ -39,6 +39,7 @@
 // buffer 1 [2D+128, 2D+256).
 #include <math.h>
 
+#include "bounded_wait.cuh"
 #include "fa_internal.cuh"
 #include "sm103_ptx.cuh"
 
@@ -50,7 +51,6 @@ constexpr int BN = kTileK;  // 128 key rows per CTA
 constexpr int kThreads = 320;
 constexpr int kWarpDrain0 = 0, kWarpSoft0 = 4, kWarpTma = 8, kWarpMma = 9;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint64_t kWaitLimitNs = 10ull * 1000 * 1000 * 1000;  // 10 s
 constexpr uint32_t kDrainBarrier = 1;                           // named barrier of the drain warps
 
 template <int D>
@@ -70,7 +70,7 @@ struct Cfg {
     static constexpr uint32_t OFF_LSE = OFF_DS + kdS_B;
     static constexpr uint32_t OFF_DD = OFF_LSE + STAGES * BM * 4;
     static constexpr uint32_t OFF_BAR = OFF_DD + STAGES * BM * 4;
-    static constexpr uint32_t kNumBars = 16 + 2 * STAGES;
+    static constexpr uint32_t kNumBars = 12 + 2 * STAGES;  // B_STAGE0 + 2 * STAGES
     static constexpr uint32_t OFF_MISC = OFF_BAR + kNumBars * 8;
     static constexpr uint32_t SMEM = OFF_MISC + 16;
     static constexpr uint32_t TM_DV = 0, TM_DK = D, TM_BUF0 = 2 * D;
@@ -91,7 +91,7 @@ enum {
     B_G4,          // dK product of iteration i done (MMA commit)
     B_ACC,         // every product done: dK / dV final (MMA commit)
     B_FINAL,       // MMA shutdown
-    B_STAGE0 = 12  // then STAGES "full" barriers, then STAGES "empty" barriers
+    B_STAGE0       // then STAGES "full" barriers, then STAGES "empty" barriers
 };
 
 struct Params {
@@ -123,41 +123,7 @@ __device__ __forceinline__ float2 unpack2(uint32_t v) {
     return __half22float2(*reinterpret_cast<__half2*>(&v));
 }
 
-// Bounded wait.  Returns false (and raises the CTA abort flag and the device
-// error word) if the phase did not complete in time or another role aborted.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                         unsigned int* err) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = ptx::globaltimer();
-    uint32_t spins = 0;
-    while (true) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-        if (++spins % 64 == 0) {
-            if (*abort_flag) return false;
-            if (ptx::globaltimer() - t0 > kWaitLimitNs) {
-                *abort_flag = 1;
-                atomicOr(err, kErrTimeout);
-                return false;
-            }
-        }
-    }
-}
-
-// Warp-uniform bounded wait: every lane waits (each gets the acquire), the
-// warp then agrees, so a timeout seen by one lane makes the whole warp leave.
-__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                              unsigned int* err) {
-    const bool ok = wait_bar(bar, parity, abort_flag, err);
-    return __all_sync(0xffffffffu, ok);
-}
-
-// Wait used while shutting down after an abort: bounded, no flag checks.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-    const uint64_t t0 = ptx::globaltimer();
-    while (!ptx::mbar_try_wait(bar, parity)) {
-        if (ptx::globaltimer() - t0 > kWaitLimitNs) return;
-    }
-}
+static_assert(B_STAGE0 == 12, "Cfg::kNumBars counts 12 named barriers before the stage ring");
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)

@@ -73,6 +73,9 @@ cudaError_t launch_bwd_sm103(int dtype, const void* Q, const void* K, const void
                              const void* dO, const Workspace& ws, void* dK, void* dV,
                              const Shape& s, cudaStream_t st);
 
+// selftest.cu
+cudaError_t launch_wait_selftest(unsigned int* err, uint64_t limit_ns, cudaStream_t st);
+
 // api.cu: argument checks and error text shared by the entry points.
 int validate_bwd_args(const void* dO, const void* Q, const void* K, const void* V, const void* O,
                       const float* LSE, const void* dQ, const void* dK, const void* dV, int B, int H,

@@ -156,6 +156,18 @@ int fa_check_device(void* stream);
 int fa_profile(int enable);
 int fa_profile_read(float* ms, int* calls);
 
+/*
+ * fa_selftest_timeout -- failure-detection self-test (not needed in normal
+ * use): launches on `stream` one CTA that waits, through the same bounded wait
+ * the backward kernel uses, on a barrier nothing ever completes, with a limit
+ * of `limit_ns` nanoseconds (0 < limit_ns <= 1e9).  The wait runs out and the
+ * kernel records a timeout in the stream's workspace error word and returns;
+ * fa_check_device(stream) then reports FA_ERR_TIMEOUT and the CUDA context
+ * stays usable.  The bounded waits of the backward are the device side of the
+ * pages' KernelError reporting (boostr flash_bwd.rs launch errors).
+ */
+int fa_selftest_timeout(unsigned long long limit_ns, void* stream);
+
 /* Thread-local text of the last error ("arg: reason"); "" if none. */
 const char* fa_last_error(void);
 

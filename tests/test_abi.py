@@ -115,3 +115,9 @@ def test_binding_rejects_host_tensors_for_device_entry_points():
         fa.fa_bwd(q, q, q, q, q, lse)
     with pytest.raises(fa.FaError, match="4-D"):
         fa.fa_bwd(q, q[0], q, q, q, lse)
+
+
+def test_selftest_rejects_bad_limit(lib):
+    assert lib.fa_selftest_timeout(0, None) == 1
+    assert fa.fa_last_error().startswith("limit_ns:")
+    assert lib.fa_selftest_timeout(2_000_000_000, None) == 1

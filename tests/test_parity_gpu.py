@@ -200,3 +200,14 @@ def test_causal_scale_and_rows_without_keys_are_finite():
     dQ, dK, dV = run_bwd(w, Q, K, V, dO, O, LSE)
     assert bool(torch.isfinite(dQ).all() and torch.isfinite(dK).all() and torch.isfinite(dV).all())
     assert bool((dQ[:, :, :130] == 0).all())
+
+
+def test_bounded_wait_timeout_is_reported_and_context_survives():
+    """A device wait that nothing completes runs out after 1 ms, the kernel returns,
+    fa_check_device reports FA_ERR_TIMEOUT once, and the next backward is correct."""
+    fa.fa_selftest_timeout(1_000_000)
+    with pytest.raises(fa.FaError) as ei:
+        fa.fa_check_device()
+    assert ei.value.status == 4
+    fa.fa_check_device()  # the record was cleared
+    check_full(Workload("after_timeout", "bf16", 1, 2, 1, 130, 130, 64, True, seed=10))
