@@ -21,14 +21,18 @@
 //   * TMA (cp.async.bulk.tensor, 128-byte swizzle) stages K, V once and Q, dO
 //     in a multi-stage ring; causal tiles that no query can see are skipped;
 //   * the dQ tile (dS K) is drained from TMEM and added to the fp32
-//     accumulator in global memory with TMA bulk reduce-adds, 64 columns per
-//     round, staged through the dS shared-memory tile (free once the dQ product
-//     ran);
-//   * warp roles: warps 0-3 drain dQ, warps 4-7 compute P and dS and run the
-//     dK / dV epilogue, warp 8 issues TMA, warp 9 owns TMEM and issues MMAs;
+//     accumulator in global memory with TMA bulk reduce-adds, staged through
+//     the dS shared-memory tile (free once the dQ product ran) and, for d = 128,
+//     the iteration's dO tile (free once the dV product ran);
+//   * warp roles: warps 0-3 drain dQ; warps 4-11 compute P and dS and run the
+//     dK / dV epilogue, two warps per TMEM lane quadrant (one per 64-query half,
+//     so each SM sub-partition has two of them to hide TMEM / shared latency);
+//     warp 12 issues TMA; warp 13 owns TMEM and issues MMAs;
 //   * two 128-column TMEM buffers alternate roles each iteration i:
-//       X = buffer[i & 1]:  S(i) -> P(i) (packed, cols 0-63) -> dQ(i)
-//       Y = buffer[~i & 1]: dP(i) -> dS(i) (packed in place, cols 0-63) -> S(i+1)
+//       X = buffer[i & 1]:  S(i) -> P(i) (packed) -> dQ(i)
+//       Y = buffer[~i & 1]: dP(i) -> dS(i) (packed in place) -> S(i+1)
+//     where "packed" puts queries [0,64) in columns [0,32) and queries [64,128)
+//     in columns [64,96) of the buffer
 //     (Y becomes X of the next iteration); the dQ product is issued first once
 //     dS(i) is ready, so its drain starts as early as possible;
 //   * every mbarrier wait is bounded: on timeout the kernel records an error
@@ -48,8 +52,12 @@ namespace {
 
 constexpr int BM = kTileQ;  // 128 query rows per iteration
 constexpr int BN = kTileK;  // 128 key rows per CTA
-constexpr int kThreads = 320;
-constexpr int kWarpDrain0 = 0, kWarpSoft0 = 4, kWarpTma = 8, kWarpMma = 9;
+static_assert(BM == 128, "the packed P / dS column layout assumes two 64-query halves");
+constexpr int kThreads = 448;
+// warps 0-3 drain dQ; warps 4-11 compute P / dS (two warps per TMEM lane quadrant, one
+// per half of the query columns); warp 12 issues TMA; warp 13 owns TMEM and issues MMAs
+constexpr int kWarpDrain0 = 0, kWarpSoft0 = 4, kNumSoftWarps = 8, kWarpTma = 12, kWarpMma = 13;
+constexpr int kHalfQ = BM / 2;  // query columns per softmax warp
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDrainBarrier = 1;                           // named barrier of the drain warps
 
@@ -82,8 +90,8 @@ enum {
     B_KV = 0,      // K, V landed (TMA)
     B_S_FULL,      // S(i) in TMEM (MMA commit)
     B_DP_FULL,     // dP(i) in TMEM (MMA commit)
-    B_P_READY,     // P(i) packed in TMEM (4 softmax warps)
-    B_DS_READY,    // dS(i) packed in TMEM and in shared memory (4 softmax warps)
+    B_P_READY,     // P(i) packed in TMEM (8 softmax warps)
+    B_DS_READY,    // dS(i) packed in TMEM and in shared memory (8 softmax warps)
     B_DS_EMPTY,    // shared dS tile free again: dQ(i) staged out of it and read by TMA (drain)
     B_DQ_FULL,     // dQ(i) in TMEM (MMA commit)
     B_DQ_EMPTY,    // dQ(i) copied out of TMEM (4 drain warps)
@@ -104,6 +112,11 @@ struct Params {
     float scale, scale_log2;
     int causal;
 };
+
+// TMEM column (relative to a buffer) of the packed 16-bit A operand for MMA k-step k
+// (queries [16k, 16k+16)): each 64-query half is packed into the first 32 columns of
+// the 64 fp32 columns it was read from.
+__device__ __forceinline__ uint32_t packed_col(int k) { return (uint32_t)((k / 4) * 64 + (k % 4) * 8); }
 
 __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -166,7 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((sbase & 1023u) != 0) atomicOr(p.err, kErrSmemAlign);
         *abort_flag = (sbase & 1023u) != 0;
         for (int i = 0; i < (int)C::kNumBars; ++i) {
-            uint32_t count = (i == B_P_READY || i == B_DS_READY || i == B_DQ_EMPTY) ? 4u : 1u;
+            uint32_t count = (i == B_P_READY || i == B_DS_READY) ? (uint32_t)kNumSoftWarps
+                             : i == B_DQ_EMPTY                 ? 4u
+                                                               : 1u;
             if (D == 128 && i >= B_STAGE0 + C::STAGES) count = 2;  // stage "empty": MMA + drain
             ptx::mbar_init(bar(i), count);
         }
@@ -254,12 +269,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t Y = tm_buf0 + 128 * ((it & 1) ^ 1);  // dP -> dS of this iteration, S of the next
                 const uint32_t sQ = sbase + C::OFF_Q + s * C::kTileQ_B;
                 const uint32_t sdO = sbase + C::OFF_DO + s * C::kTileQ_B;
-                // dV += P^T dO   (A = P^T in TMEM X[0,64): 16 query columns = 8 packed columns per step)
+                // dV += P^T dO.  A = P^T in TMEM: queries [0,64) packed in X[0,32), queries
+                // [64,128) in X[64,96); 16 queries = 8 packed columns per step.
                 if (!(ok = wait_bar(bar(B_P_READY), it & 1, abort_flag, p.err))) break;
                 ptx::tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < BM / 16; ++k)
-                    ptx::mma_ts(tmem + C::TM_DV, X + k * 8, ptx::sw128_desc(sdO + k * 2048, C::kBoxQ_B, 1024),
+                    ptx::mma_ts(tmem + C::TM_DV, X + packed_col(k), ptx::sw128_desc(sdO + k * 2048, C::kBoxQ_B, 1024),
                                 ID_KV, (it > 0 || k > 0) ? 1u : 0u);
                 ptx::mma_commit(bar(B_G3));
                 // dQ = dS K first (its drain is the longest chain), into X once the dV
@@ -272,10 +288,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mma_ss(X, ptx::sw128_desc(sdS + k * 2048, BN * 128, 1024),
                                 ptx::sw128_desc(sK + k * 2048, C::kBoxK_B, 1024), ID_Q, k > 0);
                 ptx::mma_commit(bar(B_DQ_FULL));
-                // dK += dS^T Q   (A = dS^T in TMEM Y[0,64))
+                // dK += dS^T Q   (A = dS^T in TMEM, packed like P^T, in Y)
 #pragma unroll
                 for (int k = 0; k < BM / 16; ++k)
-                    ptx::mma_ts(tmem + C::TM_DK, Y + k * 8, ptx::sw128_desc(sQ + k * 2048, C::kBoxQ_B, 1024),
+                    ptx::mma_ts(tmem + C::TM_DK, Y + packed_col(k), ptx::sw128_desc(sQ + k * 2048, C::kBoxQ_B, 1024),
                                 ID_KV, (it > 0 || k > 0) ? 1u : 0u);
                 ptx::mma_commit(bar(B_G4));
                 // Q(i), dO(i) no longer read by MMAs (for d = 128 the stage is free only once
@@ -302,48 +318,55 @@ __global__ void __launch_bounds__(kThreads, 1)
             drain_wait(bar(B_FINAL), 0);
         }
         __syncwarp();
-    } else if (warp >= kWarpSoft0 && warp < kWarpSoft0 + 4) {
-        // ------------------------------------------------------------ P / dS (one key row per thread)
-        const int t = (warp - kWarpSoft0) * 32 + lane;  // TMEM lane == key row within the tile
-        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    } else if (warp >= kWarpSoft0 && warp < kWarpSoft0 + kNumSoftWarps) {
+        // ------------------------------------------------------------ P / dS
+        // One key row per thread (TMEM lane), two warps per lane quadrant: warp half hf
+        // owns query columns [hf*64, hf*64+64) of S / dP and packs its P / dS into the
+        // first 32 of those columns, so the two warps of a quadrant never touch each
+        // other's TMEM columns.
+        const int qd = warp & 3;                          // TMEM lane quadrant
+        const int hf = (warp - kWarpSoft0) >> 2;          // query half
+        const int qh = hf * kHalfQ;                       // first query column of this warp
+        const int t = qd * 32 + lane;                     // key row within the tile
+        const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
         const int j = n0 + t;
         const bool row_valid = j < p.S_k;
-        uint8_t* sdS_row = smem + C::OFF_DS + (t >> 3) * 1024 + (t & 7) * 128;
+        // key-major rows of the shared dS tile, 128-byte swizzled MN-major; one 64-query block per half
+        uint8_t* sdS_row = smem + C::OFF_DS + hf * (BN * 128) + (t >> 3) * 1024 + (t & 7) * 128;
         bool ok = !*abort_flag;
         for (int it = 0; ok && it < n_it; ++it) {
             const int s = it % C::STAGES;
-            const uint32_t X = tm_buf0 + 128 * (it & 1) + lane_off;
-            const uint32_t Y = tm_buf0 + 128 * ((it & 1) ^ 1) + lane_off;
+            const uint32_t X = tm_buf0 + 128 * (it & 1) + lane_off + qh;
+            const uint32_t Y = tm_buf0 + 128 * ((it & 1) ^ 1) + lane_off + qh;
             int bh, m0;
             iter_coords(it, bh, m0);
-            // warp-uniform: the chosen loop holds .sync.aligned TMEM accesses; the
-            // per-element selects inside the masked loop handle each lane's own row
-            const bool mask_tile =
-                __any_sync(0xffffffffu, !row_valid || (p.causal && (n0 + BN - 1 > m0 + off)));
-            const float* sl = reinterpret_cast<const float*>(smem + C::OFF_LSE + s * BM * 4);
-            const float* sd = reinterpret_cast<const float*>(smem + C::OFF_DD + s * BM * 4);
+            const int i_lo = m0 + qh;  // first query row of this warp's columns
+            // warp-uniform: the chosen path holds .sync.aligned TMEM accesses; the per-element
+            // selects inside the masked path handle each lane's own row
+            const bool mask_tile = __any_sync(0xffffffffu, !row_valid || (p.causal && j > i_lo + off));
+            const float* sl = reinterpret_cast<const float*>(smem + C::OFF_LSE + s * BM * 4) + qh;
+            const float* sd = reinterpret_cast<const float*>(smem + C::OFF_DD + s * BM * 4) + qh;
             if (!(ok = wait_bar_warp(bar_full(s), (it / C::STAGES) & 1, abort_flag, p.err))) break;
             if (!(ok = wait_bar_warp(bar(B_S_FULL), it & 1, abort_flag, p.err))) break;
             ptx::tc_fence_after();
-            // P = exp2(S * scale*log2e - LSE*log2e), packed to 16 bits in place (X[0,64)).
-            // Masking is decided once per tile, outside the unrolled loop, so the 64
-            // independent exp chains of a chunk stay one basic block.
-            uint32_t Pp[BM / 2];
-            auto p_chunk = [&](int c, bool masked) {
-                uint32_t r[64];
-                ptx::tmem_ld32p(X + c * 64, r);
-                ptx::tmem_ld32p(X + c * 64 + 32, r + 32);
+            // P = exp2(S * scale*log2e - LSE*log2e), packed to 16 bits in place.  Masking is
+            // decided once per warp, outside the unrolled loop, so the 64 independent exp
+            // chains stay one basic block.
+            uint32_t Pp[kHalfQ / 2];
+            auto p_block = [&](bool masked) {
+                uint32_t r[kHalfQ];
+                ptx::tmem_ld32p(X, r);
+                ptx::tmem_ld32p(X + 32, r + 32);
                 ptx::tmem_wait_ld();
 #pragma unroll
-                for (int k = 0; k < 64; k += 4) {
-                    const int q = c * 64 + k;
+                for (int q = 0; q < kHalfQ; q += 4) {
                     const float4 l4 = *reinterpret_cast<const float4*>(sl + q);
-                    float x0 = ptx::ex2(fmaf(__uint_as_float(r[k + 0]), p.scale_log2, -l4.x));
-                    float x1 = ptx::ex2(fmaf(__uint_as_float(r[k + 1]), p.scale_log2, -l4.y));
-                    float x2 = ptx::ex2(fmaf(__uint_as_float(r[k + 2]), p.scale_log2, -l4.z));
-                    float x3 = ptx::ex2(fmaf(__uint_as_float(r[k + 3]), p.scale_log2, -l4.w));
+                    float x0 = ptx::ex2(fmaf(__uint_as_float(r[q + 0]), p.scale_log2, -l4.x));
+                    float x1 = ptx::ex2(fmaf(__uint_as_float(r[q + 1]), p.scale_log2, -l4.y));
+                    float x2 = ptx::ex2(fmaf(__uint_as_float(r[q + 2]), p.scale_log2, -l4.z));
+                    float x3 = ptx::ex2(fmaf(__uint_as_float(r[q + 3]), p.scale_log2, -l4.w));
                     if (masked) {
-                        const int lim = m0 + q + off;  // key j visible to query m0+q+u iff j <= lim+u
+                        const int lim = i_lo + q + off;  // key j visible to query i_lo+q+u iff j <= lim+u
                         x0 = (row_valid && (!p.causal || j <= lim + 0)) ? x0 : 0.f;
                         x1 = (row_valid && (!p.causal || j <= lim + 1)) ? x1 : 0.f;
                         x2 = (row_valid && (!p.causal || j <= lim + 2)) ? x2 : 0.f;
@@ -352,50 +375,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                     Pp[q / 2] = pack2<kBF16>(x0, x1);
                     Pp[q / 2 + 1] = pack2<kBF16>(x2, x3);
                 }
-                ptx::tmem_st32(X + c * 32, Pp + c * 32);
+                ptx::tmem_st32(X, Pp);
             };
-            if (mask_tile) {
-#pragma unroll
-                for (int c = 0; c < BM / 64; ++c) p_chunk(c, true);
-            } else {
-#pragma unroll
-                for (int c = 0; c < BM / 64; ++c) p_chunk(c, false);
-            }
+            if (mask_tile)
+                p_block(true);
+            else
+                p_block(false);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(B_P_READY));
 
-            // dS = P * (dP - D): packed in place into Y[0,64) for the dK product and
-            // into the shared dS tile (key-major rows, 128-byte swizzled MN-major) for dQ.
+            // dS = P * (dP - D): packed in place into this warp's first 32 columns of Y for
+            // the dK product, and into the shared dS tile for dQ.
             if (!(ok = wait_bar_warp(bar(B_DP_FULL), it & 1, abort_flag, p.err))) break;
             if (it > 0 && !(ok = wait_bar_warp(bar(B_DS_EMPTY), (it - 1) & 1, abort_flag, p.err))) break;
             ptx::tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < BM / 32; ++c) {
-                uint32_t r[32];
-                ptx::tmem_ld32p(Y + c * 32, r);
+            {
+                uint32_t r[kHalfQ];
+                ptx::tmem_ld32p(Y, r);
+                ptx::tmem_ld32p(Y + 32, r + 32);
                 ptx::tmem_wait_ld();
-                uint32_t pk[16];
+                uint32_t pk[kHalfQ / 2];
 #pragma unroll
-                for (int k = 0; k < 32; k += 4) {
-                    const int q = c * 32 + k;
+                for (int q = 0; q < kHalfQ; q += 4) {
                     const float4 d4 = *reinterpret_cast<const float4*>(sd + q);
                     const float2 p01 = unpack2<kBF16>(Pp[q / 2]);
                     const float2 p23 = unpack2<kBF16>(Pp[q / 2 + 1]);
-                    pk[k / 2] = pack2<kBF16>(p01.x * (__uint_as_float(r[k]) - d4.x),
-                                             p01.y * (__uint_as_float(r[k + 1]) - d4.y));
-                    pk[k / 2 + 1] = pack2<kBF16>(p23.x * (__uint_as_float(r[k + 2]) - d4.z),
-                                                 p23.y * (__uint_as_float(r[k + 3]) - d4.w));
+                    pk[q / 2] = pack2<kBF16>(p01.x * (__uint_as_float(r[q]) - d4.x),
+                                             p01.y * (__uint_as_float(r[q + 1]) - d4.y));
+                    pk[q / 2 + 1] = pack2<kBF16>(p23.x * (__uint_as_float(r[q + 2]) - d4.z),
+                                                 p23.y * (__uint_as_float(r[q + 3]) - d4.w));
                 }
-                ptx::tmem_st16(Y + c * 16, pk);  // columns already read
+                ptx::tmem_st32(Y, pk);  // columns already read
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int q0 = c * 32 + u * 8;
-                    const int blk = q0 >> 6, chunk = (q0 & 63) >> 3;
-                    *reinterpret_cast<uint4*>(sdS_row + blk * (BN * 128) + ((chunk ^ (t & 7)) << 4)) =
+                for (int u = 0; u < kHalfQ / 8; ++u)  // 8 queries = one 16-byte chunk
+                    *reinterpret_cast<uint4*>(sdS_row + ((u ^ (t & 7)) << 4)) =
                         make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-                }
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
@@ -403,14 +419,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(B_DS_READY));
         }
-        // ---- epilogue: dV and scale * dK rows to global
+        // ---- epilogue: dV and scale * dK rows to global, columns [hf*D/2, hf*D/2 + D/2)
         if (ok && n_it > 0) ok = wait_bar_warp(bar(B_ACC), 0, abort_flag, p.err);
         if (ok) {
             ptx::tc_fence_after();
             T* dVrow = static_cast<T*>(p.dV) + ((size_t)bkv * p.S_k + j) * D;
             T* dKrow = static_cast<T*>(p.dK) + ((size_t)bkv * p.S_k + j) * D;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int cc = 0; cc < D / 64; ++cc) {
+                const int c = hf * (D / 64) + cc;  // 32-column chunk
                 uint32_t rv[32], rk[32];
                 if (n_it > 0) {
                     ptx::tmem_ld32p(tmem + C::TM_DV + lane_off + c * 32, rv);
@@ -461,24 +478,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = ptx::named_bar_and(kDrainBarrier, 128, wait_bar(bar(B_DQ_FULL), it & 1, abort_flag, p.err));
             if (!ok) break;
             ptx::tc_fence_after();
-            uint32_t r[D];
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32p(X + c * 32, r + c * 32);
-            ptx::tmem_wait_ld();
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(B_DQ_EMPTY));
             // Both staging areas are free: the dQ product (reads dS) and, before it, the dV
             // product (reads dO) are complete (B_DQ_FULL); the previous bulk reduce out of the
-            // dS tile was read before B_DS_EMPTY let the next dS in.
+            // dS tile was read before B_DS_EMPTY let the next dS in.  64 columns at a time
+            // (register budget); the TMEM buffer is released after the last load, which still
+            // precedes the end of the dK and next-S products the MMA warp has queued.
 #pragma unroll
             for (int h = 0; h < D / 64; ++h) {
+                uint32_t r[64];
+                ptx::tmem_ld32p(X + h * 64, r);
+                ptx::tmem_ld32p(X + h * 64 + 32, r + 32);
+                ptx::tmem_wait_ld();
+                if (h == D / 64 - 1) {
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bar(B_DQ_EMPTY));
+                }
                 uint8_t* area = smem + (h == 0 ? C::OFF_DS : C::OFF_DO + s * C::kTileQ_B);
 #pragma unroll
                 for (int bx = 0; bx < 2; ++bx)
 #pragma unroll
                     for (int cq = 0; cq < 8; ++cq) {
-                        const int e = h * 64 + bx * 32 + cq * 4;
+                        const int e = bx * 32 + cq * 4;
                         *reinterpret_cast<uint4*>(area + bx * (BM * 128) + t * 128 + ((cq ^ (t & 7)) << 4)) =
                             make_uint4(r[e], r[e + 1], r[e + 2], r[e + 3]);
                     }
