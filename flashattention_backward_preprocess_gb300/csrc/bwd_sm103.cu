@@ -358,22 +358,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tmem_ld32p(X, r);
                 ptx::tmem_ld32p(X + 32, r + 32);
                 ptx::tmem_wait_ld();
+                const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
                 for (int q = 0; q < kHalfQ; q += 4) {
                     const float4 l4 = *reinterpret_cast<const float4*>(sl + q);
-                    float x0 = ptx::ex2(fmaf(__uint_as_float(r[q + 0]), p.scale_log2, -l4.x));
-                    float x1 = ptx::ex2(fmaf(__uint_as_float(r[q + 1]), p.scale_log2, -l4.y));
-                    float x2 = ptx::ex2(fmaf(__uint_as_float(r[q + 2]), p.scale_log2, -l4.z));
-                    float x3 = ptx::ex2(fmaf(__uint_as_float(r[q + 3]), p.scale_log2, -l4.w));
+                    float2 a = __ffma2_rn(make_float2(__uint_as_float(r[q]), __uint_as_float(r[q + 1])), sc2,
+                                          make_float2(-l4.x, -l4.y));
+                    float2 b = __ffma2_rn(make_float2(__uint_as_float(r[q + 2]), __uint_as_float(r[q + 3])), sc2,
+                                          make_float2(-l4.z, -l4.w));
+                    a = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
+                    b = make_float2(ptx::ex2(b.x), ptx::ex2(b.y));
                     if (masked) {
                         const int lim = i_lo + q + off;  // key j visible to query i_lo+q+u iff j <= lim+u
-                        x0 = (row_valid && (!p.causal || j <= lim + 0)) ? x0 : 0.f;
-                        x1 = (row_valid && (!p.causal || j <= lim + 1)) ? x1 : 0.f;
-                        x2 = (row_valid && (!p.causal || j <= lim + 2)) ? x2 : 0.f;
-                        x3 = (row_valid && (!p.causal || j <= lim + 3)) ? x3 : 0.f;
+                        a.x = (row_valid && (!p.causal || j <= lim + 0)) ? a.x : 0.f;
+                        a.y = (row_valid && (!p.causal || j <= lim + 1)) ? a.y : 0.f;
+                        b.x = (row_valid && (!p.causal || j <= lim + 2)) ? b.x : 0.f;
+                        b.y = (row_valid && (!p.causal || j <= lim + 3)) ? b.y : 0.f;
                     }
-                    Pp[q / 2] = pack2<kBF16>(x0, x1);
-                    Pp[q / 2 + 1] = pack2<kBF16>(x2, x3);
+                    Pp[q / 2] = pack2<kBF16>(a.x, a.y);
+                    Pp[q / 2 + 1] = pack2<kBF16>(b.x, b.y);
                 }
                 ptx::tmem_st32(X, Pp);
             };
@@ -402,10 +405,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float4 d4 = *reinterpret_cast<const float4*>(sd + q);
                     const float2 p01 = unpack2<kBF16>(Pp[q / 2]);
                     const float2 p23 = unpack2<kBF16>(Pp[q / 2 + 1]);
-                    pk[q / 2] = pack2<kBF16>(p01.x * (__uint_as_float(r[q]) - d4.x),
-                                             p01.y * (__uint_as_float(r[q + 1]) - d4.y));
-                    pk[q / 2 + 1] = pack2<kBF16>(p23.x * (__uint_as_float(r[q + 2]) - d4.z),
-                                                 p23.y * (__uint_as_float(r[q + 3]) - d4.w));
+                    // dP - D (one rounding, as fp32 subtraction), then times P
+                    const float2 t01 = __ffma2_rn(make_float2(d4.x, d4.y), make_float2(-1.f, -1.f),
+                                                  make_float2(__uint_as_float(r[q]), __uint_as_float(r[q + 1])));
+                    const float2 t23 = __ffma2_rn(make_float2(d4.z, d4.w), make_float2(-1.f, -1.f),
+                                                  make_float2(__uint_as_float(r[q + 2]), __uint_as_float(r[q + 3])));
+                    const float2 s01 = __fmul2_rn(p01, t01);
+                    const float2 s23 = __fmul2_rn(p23, t23);
+                    pk[q / 2] = pack2<kBF16>(s01.x, s01.y);
+                    pk[q / 2 + 1] = pack2<kBF16>(s23.x, s23.y);
                 }
                 ptx::tmem_st32(Y, pk);  // columns already read
 #pragma unroll
