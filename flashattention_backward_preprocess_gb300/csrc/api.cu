@@ -232,10 +232,16 @@ int bwd_impl(const void* dO, const void* Q, const void* K, const void* V, const 
 
 size_t elem_size(int dtype) { return dtype == FA_F32 ? 4 : 2; }
 
-// Host-buffer staging for fa_bwd_host, per (device, stream).
+// Host-buffer staging for fa_bwd_host, per (device, stream): device buffers for every
+// input and output, two copy streams (host -> device, device -> host) and one pair of
+// events per chunk of the copy / compute pipeline.
+constexpr int kHostMaxChunks = 4;
+constexpr size_t kHostChunkBytes = 16u << 20;  // input bytes per pipeline chunk (target)
 struct HostStage {
     void* base = nullptr;
     size_t bytes = 0;
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t ev_in[kHostMaxChunks] = {}, ev_done[kHostMaxChunks] = {};
 };
 std::map<std::pair<int, cudaStream_t>, HostStage> g_stage;
 
@@ -316,8 +322,15 @@ int fa_bwd_host(const void* dO, const void* Q, const void* K, const void* V, con
         return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t es = elem_size(dtype);
-    const size_t nq = (size_t)B * H * S_q * d * es, nk = (size_t)B * H_kv * S_k * d * es;
-    const size_t nl = (size_t)B * H * S_q * 4;
+    const int g = H / H_kv;
+    // Work unit = one (batch, kv head) with its g query heads.  In every tensor the units are
+    // stored one after another in (b, kv head) order, so a range of units is one contiguous
+    // slice of each tensor and a backward problem of its own (B = 1, H_kv = units, H = g units).
+    const size_t uq = (size_t)g * S_q * d * es;  // dO, Q, O, dQ bytes per unit
+    const size_t uk = (size_t)S_k * d * es;      // K, V, dK, dV bytes per unit
+    const size_t ul = (size_t)g * S_q * 4;       // LSE bytes per unit
+    const int units = B * H_kv;
+    const size_t nq = units * uq, nk = units * uk, nl = units * ul;
     // device layout: dO Q O dQ | K V dK dV | LSE, each 256-byte aligned
     size_t off[9], tot = 0;
     const size_t sz[9] = {nq, nq, nq, nq, nk, nk, nk, nk, nl};
@@ -329,43 +342,78 @@ int fa_bwd_host(const void* dO, const void* Q, const void* K, const void* V, con
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
     char* dbase = nullptr;
+    HostStage* hs = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_ws_mu);
-        HostStage& hs = g_stage[{dev, st}];
-        if (hs.bytes < tot) {
-            if (hs.base) {
+        hs = &g_stage[{dev, st}];
+        if (!hs->ev_done[kHostMaxChunks - 1]) {  // created last: set once everything exists
+            if ((!hs->s_in && (e = cudaStreamCreateWithFlags(&hs->s_in, cudaStreamNonBlocking)) != cudaSuccess) ||
+                (!hs->s_out && (e = cudaStreamCreateWithFlags(&hs->s_out, cudaStreamNonBlocking)) != cudaSuccess))
+                return cuda_fail("cudaStreamCreateWithFlags", e);
+            for (int c = 0; c < kHostMaxChunks; ++c)
+                if ((!hs->ev_in[c] && (e = cudaEventCreateWithFlags(&hs->ev_in[c], cudaEventDisableTiming)) != cudaSuccess) ||
+                    (!hs->ev_done[c] && (e = cudaEventCreateWithFlags(&hs->ev_done[c], cudaEventDisableTiming)) != cudaSuccess))
+                    return cuda_fail("cudaEventCreateWithFlags", e);
+        }
+        if (hs->bytes < tot) {
+            if (hs->base) {
                 cudaStreamSynchronize(st);
-                cudaFree(hs.base);
-                hs.base = nullptr;
-                hs.bytes = 0;
+                cudaFree(hs->base);
+                hs->base = nullptr;
+                hs->bytes = 0;
             }
-            e = cudaMalloc(&hs.base, tot);
+            e = cudaMalloc(&hs->base, tot);
             if (e != cudaSuccess) {
                 cudaGetLastError();
-                hs.base = nullptr;
+                hs->base = nullptr;
                 return fail(FA_ERR_NOMEM, "staging", cudaGetErrorString(e));
             }
-            hs.bytes = tot;
+            hs->bytes = tot;
         }
-        dbase = static_cast<char*>(hs.base);
+        dbase = static_cast<char*>(hs->base);
     }
+    // Pipeline over chunks of units: chunk c's inputs are copied on s_in while chunk c-1 runs
+    // on `stream` and chunk c-2's results are copied back on s_out.  Every chunk has its own
+    // device buffers (the full-size staging above), so no chunk waits for another's copies.
+    // (One stream per direction: splitting every copy over four streams per direction
+    // measured slower.)
+    const size_t in_bytes = 3 * nq + 2 * nk + nl;
+    int n_chunks = (int)(in_bytes / kHostChunkBytes);
+    n_chunks = n_chunks < 1 ? 1 : n_chunks > kHostMaxChunks ? kHostMaxChunks : n_chunks;
+    if (n_chunks > units) n_chunks = units;
     const void* hin[6] = {dO, Q, O, K, V, LSE};
     const int in_slot[6] = {0, 1, 2, 4, 5, 8};
-    for (int i = 0; i < 6; ++i) {
-        e = cudaMemcpyAsync(dbase + off[in_slot[i]], hin[i], sz[in_slot[i]], cudaMemcpyHostToDevice, st);
-        if (e != cudaSuccess) return cuda_fail("cudaMemcpyAsync H2D", e);
-    }
-    rc = bwd_impl(dbase + off[0], dbase + off[1], dbase + off[4], dbase + off[5], dbase + off[2],
-                  reinterpret_cast<const float*>(dbase + off[8]), dbase + off[3], dbase + off[6],
-                  dbase + off[7], B, H, H_kv, S_q, S_k, d, scale, causal, dtype, st);
-    if (rc != FA_OK) return rc;
     void* hout[3] = {dQ, dK, dV};
     const int out_slot[3] = {3, 6, 7};
-    for (int i = 0; i < 3; ++i) {
-        e = cudaMemcpyAsync(hout[i], dbase + off[out_slot[i]], sz[out_slot[i]], cudaMemcpyDeviceToHost, st);
-        if (e != cudaSuccess) return cuda_fail("cudaMemcpyAsync D2H", e);
+    auto unit_bytes = [&](int slot) { return slot < 4 ? uq : slot < 8 ? uk : ul; };
+    for (int c = 0; c < n_chunks; ++c) {
+        const int u0 = (int)((long)units * c / n_chunks), u1 = (int)((long)units * (c + 1) / n_chunks);
+        const int nu = u1 - u0;
+        for (int i = 0; i < 6; ++i) {
+            const size_t ub = unit_bytes(in_slot[i]);
+            e = cudaMemcpyAsync(dbase + off[in_slot[i]] + u0 * ub, static_cast<const char*>(hin[i]) + u0 * ub,
+                                nu * ub, cudaMemcpyHostToDevice, hs->s_in);
+            if (e != cudaSuccess) return cuda_fail("cudaMemcpyAsync H2D", e);
+        }
+        if ((e = cudaEventRecord(hs->ev_in[c], hs->s_in)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(st, hs->ev_in[c], 0)) != cudaSuccess)
+            return cuda_fail("cudaEventRecord / cudaStreamWaitEvent", e);
+        auto at = [&](int slot) { return dbase + off[slot] + u0 * unit_bytes(slot); };
+        rc = bwd_impl(at(0), at(1), at(4), at(5), at(2), reinterpret_cast<const float*>(at(8)), at(3), at(6), at(7),
+                      1, nu * g, nu, S_q, S_k, d, scale, causal, dtype, st);
+        if (rc != FA_OK) return rc;
+        if ((e = cudaEventRecord(hs->ev_done[c], st)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(hs->s_out, hs->ev_done[c], 0)) != cudaSuccess)
+            return cuda_fail("cudaEventRecord / cudaStreamWaitEvent", e);
+        for (int i = 0; i < 3; ++i) {
+            const size_t ub = unit_bytes(out_slot[i]);
+            e = cudaMemcpyAsync(static_cast<char*>(hout[i]) + u0 * ub, dbase + off[out_slot[i]] + u0 * ub, nu * ub,
+                                cudaMemcpyDeviceToHost, hs->s_out);
+            if (e != cudaSuccess) return cuda_fail("cudaMemcpyAsync D2H", e);
+        }
     }
-    e = cudaStreamSynchronize(st);
+    // s_out waited for the last chunk's compute, which waited for every input copy
+    e = cudaStreamSynchronize(hs->s_out);
     if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
     return FA_OK;
 }
@@ -446,8 +494,18 @@ void fa_shutdown(void) {
     for (auto& kv : g_ws)
         if (kv.second.base) cudaFree(kv.second.base);
     g_ws.clear();
-    for (auto& kv : g_stage)
-        if (kv.second.base) cudaFree(kv.second.base);
+    for (auto& kv : g_stage) {
+        HostStage& hs = kv.second;
+        if (hs.s_in) cudaStreamSynchronize(hs.s_in);
+        if (hs.s_out) cudaStreamSynchronize(hs.s_out);
+        if (hs.base) cudaFree(hs.base);
+        for (int c = 0; c < kHostMaxChunks; ++c) {
+            if (hs.ev_in[c]) cudaEventDestroy(hs.ev_in[c]);
+            if (hs.ev_done[c]) cudaEventDestroy(hs.ev_done[c]);
+        }
+        if (hs.s_in) cudaStreamDestroy(hs.s_in);
+        if (hs.s_out) cudaStreamDestroy(hs.s_out);
+    }
     g_stage.clear();
 }
 

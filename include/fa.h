@@ -103,10 +103,15 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int
 
 /*
  * fa_bwd_host -- fa_bwd on HOST buffers (same arguments and layouts, every
- * pointer a host pointer; pinned memory gives full copy bandwidth).  Copies
- * the inputs to device buffers cached per (device, stream), runs fa_bwd on
- * `stream`, copies dQ, dK, dV back and synchronizes `stream` before
- * returning.
+ * pointer a host pointer; pinned memory gives full copy bandwidth and lets
+ * copies overlap compute).  Copies the inputs to device buffers cached per
+ * (device, stream), runs the backward on `stream`, copies dQ, dK, dV back and
+ * returns once they are in the host buffers.  Problems with more than 32 MiB
+ * of input are split into up to 4 chunks of whole (batch, kv head) units:
+ * chunk c's inputs are copied on a library-owned stream while chunk c-1
+ * computes on `stream` and chunk c-2's results are copied back on a second
+ * library-owned stream.  Results are those of fa_bwd (dQ up to the order of
+ * its fp32 reduction).
  */
 int fa_bwd_host(const void* dO, const void* Q, const void* K, const void* V, const void* O,
                 const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv, int S_q,

@@ -192,6 +192,19 @@ def test_host_buffer_entry_point_matches_device():
     assert rel_err(f64(hQ), f64(dQ)) < 1e-2
 
 
+def test_host_buffer_entry_point_pipelined_chunks():
+    # 73 MB of input: fa_bwd_host splits the 10 (batch, kv head) units into 4 chunks of
+    # 2, 3, 2, 3 units, whose copies overlap the other chunks' compute; every unit's dK / dV
+    # must equal the single-call device result bit for bit
+    w = Workload("host_chunks", "bf16", 5, 8, 2, 2048, 2048, 128, True, seed=16)
+    Q, K, V, dO, O, LSE = prepare(w)
+    dQ, dK, dV = run_bwd(w, Q, K, V, dO, O, LSE)
+    host = [x.cpu().pin_memory() for x in (dO, Q, K, V, O, LSE)]
+    hQ, hK, hV = fa.fa_bwd_host(*host, scale=w.scale, causal=True)
+    assert torch.equal(hK, dK.cpu()) and torch.equal(hV, dV.cpu())
+    assert rel_err(f64(hQ), f64(dQ)) < 1e-2
+
+
 def test_causal_scale_and_rows_without_keys_are_finite():
     # S_q > S_k causal: the first S_q - S_k query rows see no key (LSE = -inf); their dQ is 0
     w = Workload("masked", "bf16", 1, 2, 2, 260, 130, 128, True, seed=9)
