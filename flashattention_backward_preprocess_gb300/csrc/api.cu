@@ -185,6 +185,16 @@ bool use_simt_for_16bit() {
     return v == 1;
 }
 
+// FA_FWD_KERNEL=simt: the forward helper on CUDA cores for f16 / bf16 too
+bool fwd_simt_for_16bit() {
+    static int v = -1;
+    if (v < 0) {
+        const char* e = getenv("FA_FWD_KERNEL");
+        v = (e && std::string(e) == "simt") ? 1 : 0;
+    }
+    return v == 1;
+}
+
 int bwd_impl(const void* dO, const void* Q, const void* K, const void* V, const void* O,
              const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv, int S_q,
              int S_k, int d, float scale, int causal, int dtype, cudaStream_t st) {
@@ -305,7 +315,17 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int
         (rc = check_ptr(O, "O", 16)) || (rc = check_ptr(LSE, "LSE", 4)))
         return rc;
     const Shape s = make_shape(B, H, H_kv, S_q, S_k, d, scale, causal);
-    cudaError_t e = launch_fwd_simt(dtype, Q, K, V, O, LSE, s, static_cast<cudaStream_t>(stream));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (dtype == FA_F32 || fwd_simt_for_16bit()) {
+        e = launch_fwd_simt(dtype, Q, K, V, O, LSE, s, st);
+    } else {
+        // the tensor-core forward reports bounded-wait timeouts in the stream's workspace
+        // error words (fa_check_device reads them)
+        void* base = nullptr;
+        if ((rc = get_workspace(st, 256, &base))) return rc;
+        e = launch_fwd_sm103(dtype, Q, K, V, O, LSE, static_cast<unsigned int*>(base), s, st);
+    }
     if (e != cudaSuccess) return cuda_fail("forward launch", e);
     return FA_OK;
 }

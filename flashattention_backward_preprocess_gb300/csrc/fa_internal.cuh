@@ -73,6 +73,9 @@ cudaError_t launch_bwd_sm103(int dtype, const void* Q, const void* K, const void
                              const void* dO, const Workspace& ws, void* dK, void* dV,
                              const Shape& s, cudaStream_t st);
 
+// fwd_sm103.cu (tcgen05 forward for f16 / bf16, head dim 64 or 128)
+cudaError_t launch_fwd_sm103(int dtype, const void* Q, const void* K, const void* V, void* O,
+                             float* LSE, unsigned int* err, const Shape& s, cudaStream_t st);
 // selftest.cu
 cudaError_t launch_wait_selftest(unsigned int* err, uint64_t limit_ns, cudaStream_t st);
 

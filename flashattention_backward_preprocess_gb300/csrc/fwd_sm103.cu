@@ -1,0 +1,397 @@
+// fwd_sm103.cu -- attention forward for GB300 (sm_103a), f16 / bf16, head dim 64
+// or 128: the O and LSE the backward consumes (boostr autograd_attention.rs: the
+// forward saves q, k, v, output and lse for FlashAttentionBackward).
+//
+//   s_ij = scale <Q_i, K_j> over the visible keys j (causal: j <= i + S_k - S_q)
+//   O_i  = sum_j exp(s_ij) V_j / sum_j exp(s_ij),   LSE_i = log sum_j exp(s_ij)
+// computed with the online softmax over 128-key tiles; a row that sees no key
+// gets O = 0 and LSE = -inf.
+//
+// Design:
+//   * one CTA per (128-row query tile, query head); the query tiles with the most
+//     visible key tiles start first;
+//   * S = Q K^T for key tile j runs on the 5th-generation tensor cores into one of
+//     two 128-column TMEM buffers, so S(j+1) is computed while the softmax warps
+//     work on S(j); P = exp2(x - m) is packed to 16 bits in place and is the TMEM
+//     A operand of O += P V (O accumulates in TMEM, fp32);
+//   * one softmax thread per query row (TMEM lane), logits handled in log2 units
+//     x = s * log2(e).  The running max m moves only when a tile's max exceeds it
+//     by more than 8 (P then stays <= 2^8); only then is the O row rescaled in
+//     TMEM, after the previous P V product has finished;
+//   * TMA (128-byte swizzle) loads the Q tile once and K / V through a ring;
+//     the epilogue divides O by the row sum and writes O and LSE;
+//   * warp roles: warps 0-3 softmax and epilogue, warp 4 TMA, warp 5 TMEM owner and
+//     MMA issuer; every mbarrier wait is bounded (a timeout records an error word,
+//     the other roles drop out, TMEM is freed and the kernel returns).
+#include <math.h>
+
+#include "bounded_wait.cuh"
+#include "fa_internal.cuh"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int BM = 128;  // query rows per CTA
+constexpr int BN = 128;  // key rows per step
+constexpr int kThreads = 192;
+constexpr int kWarpTma = 4, kWarpMma = 5;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.f;  // move the running max only past this margin
+
+template <int D>
+struct FCfg {
+    static constexpr int STAGES = D == 128 ? 3 : 4;
+    static constexpr int BOXES = D / 64;               // 64-column boxes per tile row
+    static constexpr uint32_t kTile_B = 128 * D * 2;   // Q, K or V tile
+    static constexpr uint32_t kBox_B = 128 * 128;      // one 64-column box of a tile
+    static constexpr uint32_t OFF_Q = 0;
+    static constexpr uint32_t OFF_K = OFF_Q + kTile_B;
+    static constexpr uint32_t OFF_V = OFF_K + STAGES * kTile_B;
+    static constexpr uint32_t OFF_BAR = OFF_V + STAGES * kTile_B;
+    static constexpr uint32_t TM_S = 0, TM_O = 256;     // S buffers [0,128), [128,256); O [256, 256+D)
+};
+
+enum {
+    F_Q = 0,      // Q tile landed (TMA)
+    F_S0,         // S(j) in buffer j % 2 (MMA commit), two slots
+    F_P0 = F_S0 + 2,  // P(j) packed in buffer j % 2 (4 softmax warps), two slots
+    F_PV = F_P0 + 2,  // O += P(j) V(j) done (MMA commit)
+    F_FINAL,      // MMA shutdown
+    F_STAGE0      // then STAGES "full" barriers, then STAGES "empty" barriers
+};
+
+struct FParams {
+    void* O;
+    float* LSE;
+    unsigned int* err;
+    int B, H, H_kv, S_q, S_k;
+    float scale_log2;
+};
+
+template <bool kBF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if (kBF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const FParams p, int causal) {
+    using C = FCfg<D>;
+    constexpr bool kBF16 = TypeTraits<T>::kId == FA_BF16;
+    constexpr int kNumBars = F_STAGE0 + 2 * C::STAGES;
+    constexpr uint32_t OFF_MISC = C::OFF_BAR + kNumBars * 8;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t sbase = ptx::smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 4);
+    auto bar = [&](int i) { return sbase + C::OFF_BAR + 8u * (uint32_t)i; };
+    auto bar_full = [&](int s) { return bar(F_STAGE0 + s); };
+    auto bar_empty = [&](int s) { return bar(F_STAGE0 + C::STAGES + s); };
+
+    // ---- work: the query tiles that see the most key tiles first, heads innermost
+    const int BH = p.B * p.H;
+    const int m_tiles = (p.S_q + BM - 1) / BM;
+    const int n_tiles = (p.S_k + BN - 1) / BN;
+    const int mt = m_tiles - 1 - (int)(blockIdx.x / BH);
+    const int bh = (int)(blockIdx.x % BH);
+    const int b = bh / p.H, h = bh % p.H;
+    const int bkv = b * p.H_kv + h / (p.H / p.H_kv);
+    const int m0 = mt * BM;
+    const int off = p.S_k - p.S_q;  // key j visible to query i iff j <= i + off (causal)
+    int n_end = n_tiles;
+    if (causal) {
+        const int last = m0 + BM - 1 + off;  // last key the tile's last row can see
+        n_end = last < 0 ? 0 : (last / BN + 1 < n_tiles ? last / BN + 1 : n_tiles);
+    }
+
+    if (threadIdx.x == 0) {
+        if ((sbase & 1023u) != 0) atomicOr(p.err, kErrSmemAlign);
+        *abort_flag = (sbase & 1023u) != 0;
+        for (int i = 0; i < kNumBars; ++i) ptx::mbar_init(bar(i), (i == F_P0 || i == F_P0 + 1) ? 4u : 1u);
+        ptx::fence_mbar_init();
+        ptx::fence_proxy_async_smem();
+    }
+    if (warp == kWarpMma) {
+        ptx::tmem_alloc(sbase + OFF_MISC + 4, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kWarpTma) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && !*abort_flag && n_end > 0) {
+            ptx::mbar_arrive_expect_tx(bar(F_Q), C::kTile_B);
+            for (int x = 0; x < C::BOXES; ++x)
+                ptx::tma_load_3d(sbase + C::OFF_Q + x * C::kBox_B, &tmQ, x * 64, m0, bh, bar(F_Q));
+            int issued = 0;
+            for (int j = 0; j < n_end; ++j) {
+                const int s = j % C::STAGES;
+                if (j >= C::STAGES && !wait_bar(bar_empty(s), ((j / C::STAGES) - 1) & 1, abort_flag, p.err)) break;
+                ptx::mbar_arrive_expect_tx(bar_full(s), 2 * C::kTile_B);
+                for (int x = 0; x < C::BOXES; ++x) {
+                    ptx::tma_load_3d(sbase + C::OFF_K + s * C::kTile_B + x * C::kBox_B, &tmK, x * 64, j * BN, bkv,
+                                     bar_full(s));
+                    ptx::tma_load_3d(sbase + C::OFF_V + s * C::kTile_B + x * C::kBox_B, &tmV, x * 64, j * BN, bkv,
+                                     bar_full(s));
+                }
+                issued = j + 1;
+            }
+            // never leave copies in flight into shared memory that is about to be released
+            drain_wait(bar(F_Q), 0);
+            for (int j = issued - C::STAGES < 0 ? 0 : issued - C::STAGES; j < issued; ++j)
+                drain_wait(bar_full(j % C::STAGES), (j / C::STAGES) & 1);
+        }
+    } else if (warp == kWarpMma) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && !*abort_flag && n_end > 0) {
+            constexpr uint32_t ID_S = ptx::idesc_f16(BM, BN, kBF16, false, false);  // S = Q K^T
+            constexpr uint32_t ID_PV = ptx::idesc_f16(BM, D, kBF16, false, true);   // O += P V (A in TMEM)
+            auto desc_add = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
+            const uint64_t dQ_k = ptx::sw128_desc(sbase + C::OFF_Q, 16, 1024);
+            const uint64_t dK_k = ptx::sw128_desc(sbase + C::OFF_K, 16, 1024);          // + stage offset
+            const uint64_t dV_mn = ptx::sw128_desc(sbase + C::OFF_V, C::kBox_B, 1024);  // + stage offset
+            // S(j) = Q K(j)^T into buffer j % 2 (both operands K-major)
+            auto gemm_s = [&](int j) {
+                const uint32_t so = (uint32_t)(j % C::STAGES) * C::kTile_B;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t ko = (k / 4) * C::kBox_B + (k % 4) * 32;
+                    ptx::mma_ss(tmem + C::TM_S + (j & 1) * 128, desc_add(dQ_k, ko), desc_add(dK_k, so + ko), ID_S,
+                                k > 0);
+                }
+                ptx::mma_commit(bar(F_S0 + (j & 1)));
+            };
+            bool ok = wait_bar(bar(F_Q), 0, abort_flag, p.err);
+            for (int j = 0; ok && j < 2 && j < n_end; ++j) {
+                if (!(ok = wait_bar(bar_full(j % C::STAGES), (j / C::STAGES) & 1, abort_flag, p.err))) break;
+                ptx::tc_fence_after();
+                gemm_s(j);
+            }
+            for (int j = 0; ok && j < n_end; ++j) {
+                const int s = j % C::STAGES;
+                // O += P(j) V(j)   (A = P packed in buffer j % 2: 16 keys = 8 packed columns per step)
+                if (!(ok = wait_bar(bar(F_P0 + (j & 1)), (j >> 1) & 1, abort_flag, p.err))) break;
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k)
+                    ptx::mma_ts(tmem + C::TM_O, tmem + C::TM_S + (j & 1) * 128 + k * 8,
+                                desc_add(dV_mn, (uint32_t)s * C::kTile_B + k * 2048), ID_PV, (j > 0 || k > 0) ? 1u : 0u);
+                ptx::mma_commit(bar(F_PV));
+                ptx::mma_commit(bar_empty(s));  // K(j), V(j) no longer read
+                if (j + 2 < n_end) {
+                    // S(j+2) into buffer j % 2 once the P V product has read P(j) out of it
+                    const int s2 = (j + 2) % C::STAGES;
+                    if (!(ok = wait_bar(bar_full(s2), ((j + 2) / C::STAGES) & 1, abort_flag, p.err))) break;
+                    if (!(ok = wait_bar(bar(F_PV), j & 1, abort_flag, p.err))) break;
+                    ptx::tc_fence_after();
+                    gemm_s(j + 2);
+                }
+            }
+            // no MMA may still write TMEM when it is released
+            ptx::mma_commit(bar(F_FINAL));
+            drain_wait(bar(F_FINAL), 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int t = warp * 32 + lane;  // TMEM lane == query row within the tile
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const int i = m0 + t;
+        const bool row_valid = i < p.S_q;
+        float m_run = -INFINITY;  // running max of x = s * log2(e), moved lazily
+        float l_run = 0.f;        // sum of exp2(x - m_run)
+        bool ok = !*abort_flag;
+        for (int j = 0; ok && j < n_end; ++j) {
+            const uint32_t buf = tmem + C::TM_S + (j & 1) * 128 + lane_off;
+            const int n0 = j * BN;
+            // warp-uniform: the chosen path holds .sync.aligned TMEM accesses
+            const bool masked = __any_sync(0xffffffffu, n0 + BN > p.S_k || (causal && n0 + BN - 1 > i + off));
+            if (!(ok = wait_bar_warp(bar(F_S0 + (j & 1)), (j >> 1) & 1, abort_flag, p.err))) break;
+            ptx::tc_fence_after();
+            uint32_t r[BN];
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) ptx::tmem_ld32p(buf + c * 32, r + c * 32);
+            ptx::tmem_wait_ld();
+            float x[BN];
+            float mx = -INFINITY;
+            if (masked) {
+                const int lim = causal ? i + off - n0 : BN;  // column c visible iff c <= lim (causal)
+                const int kend = p.S_k - n0;                 // and c < kend
+#pragma unroll
+                for (int c = 0; c < BN; ++c) {
+                    x[c] = (c < kend && c <= lim) ? __uint_as_float(r[c]) * p.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, x[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < BN; ++c) {
+                    x[c] = __uint_as_float(r[c]) * p.scale_log2;
+                    mx = fmaxf(mx, x[c]);
+                }
+            }
+            // lazy running max: move it only when this tile exceeds it by more than the margin
+            float alpha = 1.f;
+            const bool rescale = mx > m_run + kRescaleLog2;
+            if (rescale) {
+                alpha = m_run == -INFINITY ? 0.f : ptx::ex2(m_run - mx);
+                m_run = mx;
+            }
+            const float m_use = m_run == -INFINITY ? 0.f : m_run;  // rows with nothing visible yet: P = 0
+            float sum = 0.f;
+            uint32_t Pp[BN / 2];
+#pragma unroll
+            for (int c = 0; c < BN; c += 2) {
+                const float p0 = ptx::ex2(x[c] - m_use), p1 = ptx::ex2(x[c + 1] - m_use);
+                sum += p0 + p1;
+                Pp[c / 2] = pack2<kBF16>(p0, p1);
+            }
+            l_run = l_run * alpha + sum;
+            ptx::tmem_st32(buf, Pp);  // packed P into columns [0, 64): already read
+            ptx::tmem_st32(buf + 32, Pp + 32);
+            // rescale the O row before the next P V product accumulates into it
+            if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+                if (!(ok = wait_bar_warp(bar(F_PV), (j - 1) & 1, abort_flag, p.err))) break;
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    ptx::tmem_ld32p(tmem + C::TM_O + lane_off + c * 32, o);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                    ptx::tmem_st32(tmem + C::TM_O + lane_off + c * 32, o);
+                }
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(F_P0 + (j & 1)));
+        }
+        // ---- epilogue: O = acc / l, LSE = (m + log2 l) * ln 2
+        if (ok && n_end > 0) ok = wait_bar_warp(bar(F_PV), (n_end - 1) & 1, abort_flag, p.err);
+        if (ok) {
+            ptx::tc_fence_after();
+            const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+            T* Orow = static_cast<T*>(p.O) + ((size_t)bh * p.S_q + i) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                if (n_end > 0) {
+                    ptx::tmem_ld32p(tmem + C::TM_O + lane_off + c * 32, o);
+                    ptx::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) o[k] = 0u;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        w4[k] = pack2<kBF16>(__uint_as_float(o[u * 8 + 2 * k]) * inv_l,
+                                             __uint_as_float(o[u * 8 + 2 * k + 1]) * inv_l);
+                    if (row_valid) *reinterpret_cast<uint4*>(Orow + c * 32 + u * 8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+            }
+            if (row_valid)
+                p.LSE[(size_t)bh * p.S_q + i] = l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == kWarpMma) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// 3-D view [heads][rows][D] of a [B, heads, rows, D] 16-bit tensor: 64-column x 128-row
+// boxes with 128-byte swizzle (rows past the end read as zeros).
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int heads, int rows, int D) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)heads};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)rows * D * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename T, int D>
+cudaError_t launch_t(const void* Q, const void* K, const void* V, void* O, float* LSE, unsigned int* err,
+                     const Shape& s, cudaStream_t st) {
+    using C = FCfg<D>;
+    constexpr uint32_t kSmem = C::OFF_BAR + (F_STAGE0 + 2 * C::STAGES) * 8 + 16;
+    static_assert(kSmem <= 232448, "shared memory budget");
+    const CUtensorMapDataType dt =
+        TypeTraits<T>::kId == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUtensorMap tq, tk, tv;
+    if (!make_map(&tq, Q, dt, s.B * s.H, s.S_q, D) || !make_map(&tk, K, dt, s.B * s.H_kv, s.S_k, D) ||
+        !make_map(&tv, V, dt, s.B * s.H_kv, s.S_k, D))
+        return cudaErrorInvalidValue;
+    FParams p;
+    p.O = O;
+    p.LSE = LSE;
+    p.err = err;
+    p.B = s.B;
+    p.H = s.H;
+    p.H_kv = s.H_kv;
+    p.S_q = s.S_q;
+    p.S_k = s.S_k;
+    p.scale_log2 = s.scale * 1.4426950408889634f;
+    auto kern = fwd_sm103_kernel<T, D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    if (e != cudaSuccess) return e;
+    const long grid = (long)((s.S_q + BM - 1) / BM) * s.B * s.H;
+    kern<<<(unsigned)grid, kThreads, kSmem, st>>>(tq, tk, tv, p, s.causal);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_sm103(int dtype, const void* Q, const void* K, const void* V, void* O, float* LSE,
+                            unsigned int* err, const Shape& s, cudaStream_t st) {
+    if (s.d == 64) {
+        if (dtype == FA_F16) return launch_t<__half, 64>(Q, K, V, O, LSE, err, s, st);
+        if (dtype == FA_BF16) return launch_t<__nv_bfloat16, 64>(Q, K, V, O, LSE, err, s, st);
+    } else if (s.d == 128) {
+        if (dtype == FA_F16) return launch_t<__half, 128>(Q, K, V, O, LSE, err, s, st);
+        if (dtype == FA_BF16) return launch_t<__nv_bfloat16, 128>(Q, K, V, O, LSE, err, s, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace fa
