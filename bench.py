@@ -229,6 +229,39 @@ def run_reference(args, world, rank):
     return 0
 
 
+def run_forward(args, fa, w, Q, K, V, O, LSE, flush, stream, world, rank, device):
+    """The forward (O and LSE the backward consumes) on the bench workload: CUDA events per
+    call, L2 flushed between calls; 4·B·H·S_q·S_k·d flops, halved for causal."""
+    for _ in range(args.warmup):
+        fa.fa_fwd(Q, K, V, scale=w.scale, causal=w.causal, O=O, LSE=LSE)
+    torch.cuda.synchronize(device)
+    fa.fa_check_device()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        fa.fa_fwd(Q, K, V, scale=w.scale, causal=w.causal, O=O, LSE=LSE)
+        ends[i].record(stream)
+    torch.cuda.synchronize(device)
+    fa.fa_check_device()
+    ms = max_over_ranks(statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends)), world, device)
+    flops = 4.0 * w.B * w.H * w.S_q * w.S_k * w.d * (0.5 if w.causal else 1.0)
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    value = world * flops / (ms / 1e3) / 1e12
+    if rank == 0:
+        print(json.dumps({"metric": "attn-forward TFLOP/s (causal-adjusted)", "value": value, "unit": "TFLOP/s",
+                          "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                          "higher_is_better": True, "dtype": w.dtype, "data": "synthetic",
+                          "roofline": {"bound": "tensor", "achieved": value / world, "peak": peak,
+                                       "unit": "TFLOP/s", "frac": value / world / peak,
+                                       "peak_source": f"{peak_src} bf16_tflops (burst)"},
+                          "config": {"workload": w.name, "l2": "flushed between calls (256 MiB write)"}}),
+              flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -241,6 +274,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seq", type=int, default=0,
                     help="reference arm: limit the sampled sequence length (0 = the workload's)")
+    ap.add_argument("--forward", action="store_true",
+                    help="time the forward (fa_fwd) on the same workload instead of the backward")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -261,6 +296,8 @@ def main():
     dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
+    if args.forward:
+        return run_forward(args, fa, w, Q, K, V, O, LSE, flush, stream, world, rank, device)
 
     for _ in range(args.warmup):
         fa.fa_bwd(dO, Q, K, V, O, LSE, scale=w.scale, causal=w.causal, dQ=dQ, dK=dK, dV=dV)

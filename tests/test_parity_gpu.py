@@ -170,16 +170,25 @@ def test_preprocess_entry_point(dt, d, S):
     assert float(np.max(np.abs(f64(D) - ref))) <= 1e-5 * scale
 
 
-@pytest.mark.parametrize("dt,causal,S_q,S_k,d", [("bf16", True, 300, 300, 128), ("f16", False, 129, 200, 64),
-                                                 ("f32", True, 100, 160, 64)])
+@pytest.mark.parametrize("dt,causal,S_q,S_k,d", [
+    ("bf16", True, 300, 300, 128), ("f16", False, 129, 200, 64), ("f32", True, 100, 160, 64),
+    # tensor-core forward: one tile, several tiles with the diagonal, keys past the queries,
+    # rows that see no key (S_q > S_k, causal), a single element
+    ("bf16", False, 128, 128, 128), ("bf16", True, 1000, 1000, 128), ("f16", True, 130, 1030, 128),
+    ("bf16", True, 260, 130, 128), ("bf16", False, 200, 700, 64), ("f16", False, 1, 1, 64)])
 def test_forward_helper(dt, causal, S_q, S_k, d):
     w = Workload("fwd", dt, 1, 4, 2, S_q, S_k, d, causal, seed=8)
     Q, K, V, _ = make_inputs(w)
     O, LSE = fa.fa_fwd(Q.cuda(), K.cuda(), V.cuda(), scale=w.scale, causal=causal)
     torch.cuda.synchronize()
+    fa.fa_check_device()
     O64, L64 = oracle.ref_fwd(f64(Q), f64(K), f64(V), w.scale, causal)
+    assert bool(torch.isfinite(O).all())
     assert rel_err(f64(O), O64) <= TOL[dt]
-    assert float(np.max(np.abs(f64(LSE) - L64))) <= 1e-4
+    lse, fin = f64(LSE), np.isfinite(L64)
+    assert bool(np.all(np.isneginf(lse[~fin]))) and bool(np.all(np.isfinite(lse[fin])))
+    if fin.any():
+        assert float(np.max(np.abs(lse[fin] - L64[fin]))) <= 1e-4
 
 
 def test_host_buffer_entry_point_matches_device():
