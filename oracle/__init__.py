@@ -8,12 +8,13 @@ The arithmetic lives in ``fa_ref.c`` (plain C loops in double precision, see
 its header for the definitions and the pages they follow).  This module
 compiles it with gcc on first use and exposes numpy wrappers.
 
-Functions (all take / return float64 numpy arrays, layouts [B, H, S, d]):
-    ref_fwd(Q, K, V, scale, causal)                    -> (O, LSE)
-    ref_preprocess(dO, O)                              -> D
-    ref_bwd(dO, Q, K, V, O, LSE, scale, causal)        -> (dQ, dK, dV, D)
-    ref_dq_rows(..., rows)                             -> dQ rows
-    ref_dkv_rows(..., rows)                            -> (dK rows, dV rows)
+Functions (all take / return float64 numpy arrays, layouts [B, H, S, d];
+``window`` is the sliding-window size, 0 for none):
+    ref_fwd(Q, K, V, scale, causal, window=0)              -> (O, LSE)
+    ref_preprocess(dO, O)                                  -> D
+    ref_bwd(dO, Q, K, V, O, LSE, scale, causal, window=0)  -> (dQ, dK, dV, D)
+    ref_dq_rows(..., rows, scale, causal, window=0)        -> dQ rows
+    ref_dkv_rows(..., rows, scale, causal, window=0)       -> (dK rows, dV rows)
 """
 from __future__ import annotations
 
@@ -51,11 +52,11 @@ def open_library(path: str):
     P = ctypes.c_void_p
     I = ctypes.c_int
     Dbl = ctypes.c_double
-    lib.fa_ref_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, Dbl, I]
+    lib.fa_ref_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, Dbl, I, I]
     lib.fa_ref_preprocess.argtypes = [P, P, P, ctypes.c_long, I]
-    lib.fa_ref_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, Dbl, I]
-    lib.fa_ref_dq_rows.argtypes = [P, P, P, P, P, P, P, I, P, I, I, I, I, I, I, Dbl, I]
-    lib.fa_ref_dkv_rows.argtypes = [P, P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, Dbl, I]
+    lib.fa_ref_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, Dbl, I, I]
+    lib.fa_ref_dq_rows.argtypes = [P, P, P, P, P, P, P, I, P, I, I, I, I, I, I, Dbl, I, I]
+    lib.fa_ref_dkv_rows.argtypes = [P, P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, Dbl, I, I]
     lib.fa_ref_num_threads.restype = I
     return lib
 
@@ -83,6 +84,13 @@ def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
+def _window(window) -> int:
+    w = int(window)
+    if w < 0:
+        raise ValueError(f"window must be >= 0, got {w}")
+    return w
+
+
 def _dims(Q, K):
     B, H, S_q, d = Q.shape
     Bk, H_kv, S_k, dk = K.shape
@@ -91,13 +99,13 @@ def _dims(Q, K):
     return B, H, H_kv, S_q, S_k, d
 
 
-def ref_fwd(Q, K, V, scale: float, causal: bool):
+def ref_fwd(Q, K, V, scale: float, causal: bool, window: int = 0):
     Q, K, V = _f64(Q), _f64(K), _f64(V)
     B, H, H_kv, S_q, S_k, d = _dims(Q, K)
     O = np.empty((B, H, S_q, d))
     LSE = np.empty((B, H, S_q))
     _load().fa_ref_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE),
-                       B, H, H_kv, S_q, S_k, d, float(scale), int(bool(causal)))
+                       B, H, H_kv, S_q, S_k, d, float(scale), int(bool(causal)), _window(window))
     return O, LSE
 
 
@@ -109,7 +117,7 @@ def ref_preprocess(dO, O):
     return D
 
 
-def ref_bwd(dO, Q, K, V, O, LSE, scale: float, causal: bool):
+def ref_bwd(dO, Q, K, V, O, LSE, scale: float, causal: bool, window: int = 0):
     dO, Q, K, V, O, LSE = (_f64(x) for x in (dO, Q, K, V, O, LSE))
     B, H, H_kv, S_q, S_k, d = _dims(Q, K)
     dQ = np.empty_like(Q)
@@ -118,11 +126,11 @@ def ref_bwd(dO, Q, K, V, O, LSE, scale: float, causal: bool):
     D = np.empty((B, H, S_q))
     _load().fa_ref_bwd(_ptr(dO), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE),
                        _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(D),
-                       B, H, H_kv, S_q, S_k, d, float(scale), int(bool(causal)))
+                       B, H, H_kv, S_q, S_k, d, float(scale), int(bool(causal)), _window(window))
     return dQ, dK, dV, D
 
 
-def ref_dq_rows(dO, Q, K, V, O, LSE, rows, scale: float, causal: bool):
+def ref_dq_rows(dO, Q, K, V, O, LSE, rows, scale: float, causal: bool, window: int = 0):
     """dQ for flat query rows (b*H + h)*S_q + i."""
     dO, Q, K, V, O, LSE = (_f64(x) for x in (dO, Q, K, V, O, LSE))
     B, H, H_kv, S_q, S_k, d = _dims(Q, K)
@@ -130,11 +138,12 @@ def ref_dq_rows(dO, Q, K, V, O, LSE, rows, scale: float, causal: bool):
     out = np.empty((rows.size, d))
     _load().fa_ref_dq_rows(_ptr(dO), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE),
                            _ptr(rows), int(rows.size), _ptr(out),
-                           B, H, H_kv, S_q, S_k, d, float(scale), int(bool(causal)))
+                           B, H, H_kv, S_q, S_k, d, float(scale), int(bool(causal)),
+                           _window(window))
     return out
 
 
-def ref_dkv_rows(dO, Q, K, V, O, LSE, rows, scale: float, causal: bool):
+def ref_dkv_rows(dO, Q, K, V, O, LSE, rows, scale: float, causal: bool, window: int = 0):
     """dK, dV for flat key rows (b*H_kv + hk)*S_k + j (summed over the group)."""
     dO, Q, K, V, O, LSE = (_f64(x) for x in (dO, Q, K, V, O, LSE))
     B, H, H_kv, S_q, S_k, d = _dims(Q, K)
@@ -143,5 +152,6 @@ def ref_dkv_rows(dO, Q, K, V, O, LSE, rows, scale: float, causal: bool):
     dv = np.empty((rows.size, d))
     _load().fa_ref_dkv_rows(_ptr(dO), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE),
                             _ptr(rows), int(rows.size), _ptr(dk), _ptr(dv),
-                            B, H, H_kv, S_q, S_k, d, float(scale), int(bool(causal)))
+                            B, H, H_kv, S_q, S_k, d, float(scale), int(bool(causal)),
+                            _window(window))
     return dk, dv

@@ -18,8 +18,15 @@
  *   query head h reads key/value head hk = h / (H / H_kv)  (consecutive
  *   grouping; the pages only fix that dK, dV have H_kv heads).
  *
- *   mask(i, j): non-causal -> every j < S_k; causal -> j <= i + (S_k - S_q)
- *   (bottom-right alignment; equal to j <= i when S_q == S_k).
+ *   mask(i, j): query i sits at key position p_i = i + (S_k - S_q)
+ *   (bottom-right alignment; p_i = i when S_q == S_k).
+ *     non-causal -> every j < S_k;  causal -> j <= p_i.
+ *     sliding window w > 0 (boostr autograd_attention.rs, window_size in
+ *     FlashAttentionConfig; 0 means no window): additionally p_i - j < w,
+ *     and when not causal also j - p_i < w.  A causal query therefore sees
+ *     at most its w most recent keys, itself included; a non-causal one
+ *     the keys less than w positions away on either side.  The pages name
+ *     the parameter but not its exact band; this is the plain reading.
  *
  *   forward:   S_ij   = scale * <Q_i, K_j>
  *              LSE_i  = log sum_{j allowed} exp(S_ij)   (natural log,
@@ -54,11 +61,13 @@
 #define IDX4(b, h, i, c, NH, S, d) ((((size_t)(b) * (NH) + (h)) * (S) + (i)) * (size_t)(d) + (c))
 #define IDX3(b, h, i, NH, S) ((((size_t)(b) * (NH) + (h)) * (S)) + (i))
 
-/* Is key j visible to query i?  Causal uses bottom-right alignment. */
-static int allowed(long i, long j, int S_q, int S_k, int causal) {
+/* Is key j visible to query i?  Bottom-right alignment; window 0 = none. */
+static int allowed(long i, long j, int S_q, int S_k, int causal, int window) {
     if (j < 0 || j >= S_k) return 0;
+    const long p = i + (long)(S_k - S_q);
+    if (window > 0 && (p - j >= window || (!causal && j - p >= window))) return 0;
     if (!causal) return 1;
-    return j <= i + (long)(S_k - S_q);
+    return j <= p;
 }
 
 static double dot(const double* a, const double* b, int d) {
@@ -77,7 +86,8 @@ int fa_ref_num_threads(void) {
 
 /* Forward: O and LSE from Q, K, V (definition above). */
 void fa_ref_fwd(const double* Q, const double* K, const double* V, double* O, double* LSE,
-                int B, int H, int H_kv, int S_q, int S_k, int d, double scale, int causal) {
+                int B, int H, int H_kv, int S_q, int S_k, int d, double scale, int causal,
+                int window) {
     const int g = H / H_kv;
 #pragma omp parallel for collapse(2) schedule(dynamic)
     for (int b = 0; b < B; ++b)
@@ -88,7 +98,7 @@ void fa_ref_fwd(const double* Q, const double* K, const double* V, double* O, do
                 const double* q = Q + IDX4(b, h, i, 0, H, S_q, d);
                 double m = -INFINITY;
                 for (int j = 0; j < S_k; ++j) {
-                    if (!allowed(i, j, S_q, S_k, causal)) { s[j] = -INFINITY; continue; }
+                    if (!allowed(i, j, S_q, S_k, causal, window)) { s[j] = -INFINITY; continue; }
                     s[j] = scale * dot(q, K + IDX4(b, hk, j, 0, H_kv, S_k, d), d);
                     if (s[j] > m) m = s[j];
                 }
@@ -122,7 +132,7 @@ void fa_ref_preprocess(const double* dO, const double* O, double* D, long R, int
 void fa_ref_bwd(const double* dO, const double* Q, const double* K, const double* V,
                 const double* O, const double* LSE, double* dQ, double* dK, double* dV,
                 double* D_out, int B, int H, int H_kv, int S_q, int S_k, int d, double scale,
-                int causal) {
+                int causal, int window) {
     const int g = H / H_kv;
     memset(dQ, 0, sizeof(double) * (size_t)B * H * S_q * d);
     memset(dK, 0, sizeof(double) * (size_t)B * H_kv * S_k * d);
@@ -142,7 +152,7 @@ void fa_ref_bwd(const double* dO, const double* Q, const double* K, const double
                     const double Di = dot(g_o, o, d);
                     if (D_out) D_out[IDX3(b, h, i, H, S_q)] = Di;
                     for (int j = 0; j < S_k; ++j) {
-                        if (!allowed(i, j, S_q, S_k, causal)) { p[j] = 0.0; ds[j] = 0.0; continue; }
+                        if (!allowed(i, j, S_q, S_k, causal, window)) { p[j] = 0.0; ds[j] = 0.0; continue; }
                         const double sij = scale * dot(q, K + IDX4(b, hk, j, 0, H_kv, S_k, d), d);
                         p[j] = exp(sij - lse);
                         const double dpij = dot(g_o, V + IDX4(b, hk, j, 0, H_kv, S_k, d), d);
@@ -171,7 +181,7 @@ void fa_ref_bwd(const double* dO, const double* Q, const double* K, const double
 void fa_ref_dq_rows(const double* dO, const double* Q, const double* K, const double* V,
                     const double* O, const double* LSE, const long* rows, int nrows,
                     double* dQ_rows, int B, int H, int H_kv, int S_q, int S_k, int d,
-                    double scale, int causal) {
+                    double scale, int causal, int window) {
     (void)B;
     const int g = H / H_kv;
 #pragma omp parallel for schedule(dynamic)
@@ -188,7 +198,7 @@ void fa_ref_dq_rows(const double* dO, const double* Q, const double* K, const do
         double* dq = dQ_rows + (size_t)r * d;
         for (int c = 0; c < d; ++c) dq[c] = 0.0;
         for (int j = 0; j < S_k; ++j) {
-            if (!allowed(i, j, S_q, S_k, causal)) continue;
+            if (!allowed(i, j, S_q, S_k, causal, window)) continue;
             const double* k = K + IDX4(b, hk, j, 0, H_kv, S_k, d);
             const double pij = exp(scale * dot(q, k, d) - lse);
             const double dsij = pij * (dot(g_o, V + IDX4(b, hk, j, 0, H_kv, S_k, d), d) - Di);
@@ -202,7 +212,7 @@ void fa_ref_dq_rows(const double* dO, const double* Q, const double* K, const do
 void fa_ref_dkv_rows(const double* dO, const double* Q, const double* K, const double* V,
                      const double* O, const double* LSE, const long* rows, int nrows,
                      double* dK_rows, double* dV_rows, int B, int H, int H_kv, int S_q,
-                     int S_k, int d, double scale, int causal) {
+                     int S_k, int d, double scale, int causal, int window) {
     (void)B;
     const int g = H / H_kv;
 #pragma omp parallel for schedule(dynamic)
@@ -218,7 +228,7 @@ void fa_ref_dkv_rows(const double* dO, const double* Q, const double* K, const d
         for (int c = 0; c < d; ++c) { dk[c] = 0.0; dv[c] = 0.0; }
         for (int h = hk * g; h < (hk + 1) * g; ++h)
             for (int i = 0; i < S_q; ++i) {
-                if (!allowed(i, j, S_q, S_k, causal)) continue;
+                if (!allowed(i, j, S_q, S_k, causal, window)) continue;
                 const double* q = Q + IDX4(b, h, i, 0, H, S_q, d);
                 const double* g_o = dO + IDX4(b, h, i, 0, H, S_q, d);
                 const double Di = dot(g_o, O + IDX4(b, h, i, 0, H, S_q, d), d);

@@ -17,8 +17,10 @@ MUTANTS = {
     "dq_sign": ("dq[c] += scale * ds[j] * k[c];", "dq[c] -= scale * ds[j] * k[c];"),
     "dv_wrong_operand": ("dv[c] += p[j] * g_o[c];", "dv[c] += p[j] * q[c];"),
     "dk_missing_scale": ("dk[c] += scale * ds[j] * q[c];", "dk[c] += ds[j] * q[c];"),
-    "causal_off_by_one": ("return j <= i + (long)(S_k - S_q);", "return j < i + (long)(S_k - S_q);"),
-    "causal_top_left": ("return j <= i + (long)(S_k - S_q);", "return j <= i;"),
+    "causal_off_by_one": ("return j <= p;", "return j < p;"),
+    "causal_top_left": ("const long p = i + (long)(S_k - S_q);", "const long p = i;"),
+    "window_off_by_one": ("p - j >= window ||", "p - j > window ||"),
+    "window_one_sided": ("(p - j >= window || (!causal && j - p >= window))", "(p - j >= window)"),
     "group_interleaved": ("for (int h = hk * g; h < (hk + 1) * g; ++h)\n                for (int i = 0; i < S_q; ++i) {\n                    const double* q",
                           "for (int h = hk; h < H; h += H_kv)\n                for (int i = 0; i < S_q; ++i) {\n                    const double* q"),
     "lse_ignored": ("p[j] = exp(sij - lse);", "p[j] = exp(sij);"),
@@ -40,6 +42,9 @@ PIN_CALLS = [
     lambda: pins.test_gqa_is_sum_over_group(True),
     lambda: pins.test_sampled_rows_match_full_backward(True),
     lambda: pins.test_sampled_rows_match_full_backward(False),
+    lambda: [pins.test_window_matches_torch_sdpa_band(s) for s in pins.WSHAPES],
+    lambda: pins.test_window_single_query_is_trailing_slice(True),
+    lambda: pins.test_window_noncausal_first_row_is_leading_slice(),
 ]
 
 

@@ -274,3 +274,172 @@ def test_sampled_rows_match_full_backward(causal):
     dk, dv = oracle.ref_dkv_rows(dO, Q, K, V, O, LSE, krows, 0.3, causal)
     np.testing.assert_allclose(dk, dK.reshape(-1, d)[krows], rtol=1e-13, atol=1e-14)
     np.testing.assert_allclose(dv, dV.reshape(-1, d)[krows], rtol=1e-13, atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# Sliding window (window_size > 0).  Reading: query i sits at key position
+# p_i = i + S_k - S_q; a causal query sees keys p_i - w < j <= p_i, a
+# non-causal one keys with |j - p_i| < w.
+
+def _band_torch(S_q, S_k, causal, window):
+    """The visible set as a band of the all-ones matrix cut by torch.tril/triu
+    (diagonal offsets instead of per-element index tests)."""
+    off = S_k - S_q
+    m = torch.ones(S_q, S_k, dtype=torch.bool)
+    if causal:
+        m = m.tril(diagonal=off)
+    if window > 0:
+        m = m.triu(diagonal=off - window + 1)
+        if not causal:
+            m = m.tril(diagonal=off + window - 1)
+    return m
+
+
+def _sdpa_band_grads(Q, K, V, dO, scale, mask):
+    g = Q.shape[1] // K.shape[1]
+    q = torch.tensor(Q, requires_grad=True)
+    k = torch.tensor(K, requires_grad=True)
+    v = torch.tensor(V, requires_grad=True)
+    o = F.scaled_dot_product_attention(q, k.repeat_interleave(g, dim=1), v.repeat_interleave(g, dim=1),
+                                       attn_mask=mask, scale=scale)
+    o.backward(torch.tensor(dO))
+    return q.grad.numpy(), k.grad.numpy(), v.grad.numpy(), o.detach().numpy()
+
+
+WSHAPES = [
+    # B, H, H_kv, S_q, S_k, d, causal, window   (every row keeps at least one key)
+    (1, 2, 1, 9, 9, 4, True, 3),
+    (1, 2, 2, 9, 9, 4, False, 3),
+    (1, 4, 2, 7, 12, 8, True, 4),     # S_q < S_k
+    (1, 2, 1, 12, 7, 4, False, 6),    # S_q > S_k, non-causal band
+    (2, 4, 1, 17, 17, 8, True, 1),
+    (1, 2, 1, 20, 20, 8, False, 7),
+    (1, 2, 2, 5, 5, 4, True, 5),      # window = S: same as plain causal
+]
+
+
+@pytest.mark.parametrize("shape", WSHAPES)
+def test_window_matches_torch_sdpa_band(shape):
+    B, H, H_kv, S_q, S_k, d, causal, w = shape
+    rng = np.random.default_rng(23)
+    Q, K, V = _rand(rng, B, H, S_q, d), _rand(rng, B, H_kv, S_k, d), _rand(rng, B, H_kv, S_k, d)
+    dO = _rand(rng, B, H, S_q, d)
+    scale = 1.0 / math.sqrt(d)
+    O, LSE = oracle.ref_fwd(Q, K, V, scale, causal, w)
+    dQ, dK, dV, _ = oracle.ref_bwd(dO, Q, K, V, O, LSE, scale, causal, w)
+    tq, tk, tv, to = _sdpa_band_grads(Q, K, V, dO, scale, _band_torch(S_q, S_k, causal, w))
+    np.testing.assert_allclose(O, to, rtol=1e-12, atol=1e-12)
+    for name, a, b in (("dQ", dQ, tq), ("dK", dK, tk), ("dV", dV, tv)):
+        np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-11, err_msg=name)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_window_single_query_is_trailing_slice(causal):
+    """S_q = 1 sits at the last key: a window w keeps exactly the last w keys, so
+    the result is unmasked attention over K[S_k-w:], V[S_k-w:] and the other
+    keys get zero gradient."""
+    rng = np.random.default_rng(24)
+    B, H, H_kv, S_k, d, w = 1, 2, 1, 13, 8, 5
+    Q, dO = _rand(rng, B, H, 1, d), _rand(rng, B, H, 1, d)
+    K, V = _rand(rng, B, H_kv, S_k, d), _rand(rng, B, H_kv, S_k, d)
+    O, LSE = oracle.ref_fwd(Q, K, V, 0.4, causal, w)
+    dQ, dK, dV, _ = oracle.ref_bwd(dO, Q, K, V, O, LSE, 0.4, causal, w)
+    tq, tk, tv, to = _sdpa_band_grads(Q, K[:, :, -w:], V[:, :, -w:], dO, 0.4, None)
+    np.testing.assert_allclose(O, to, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dQ, tq, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dK[:, :, -w:], tk, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dV[:, :, -w:], tv, rtol=1e-10, atol=1e-12)
+    assert np.all(dK[:, :, :-w] == 0) and np.all(dV[:, :, :-w] == 0)
+
+
+def test_window_noncausal_first_row_is_leading_slice():
+    """Non-causal, S_q = S_k: query 0 sees keys 0 .. w-1 and no others."""
+    rng = np.random.default_rng(25)
+    B, H, S, d, w = 1, 2, 11, 8, 4
+    Q, K, V, dO = (_rand(rng, B, H, S, d) for _ in range(4))
+    O, LSE = oracle.ref_fwd(Q, K, V, 0.5, False, w)
+    _, _, _, to = _sdpa_band_grads(Q[:, :, :1], K[:, :, :w], V[:, :, :w], dO[:, :, :1], 0.5, None)
+    np.testing.assert_allclose(O[:, :, :1], to, rtol=1e-12, atol=1e-13)
+    rows = np.array([0, S])   # query 0 of heads 0 and 1
+    tq = _sdpa_band_grads(Q[:, :, :1], K[:, :, :w], V[:, :, :w], dO[:, :, :1], 0.5, None)[0]
+    np.testing.assert_allclose(oracle.ref_dq_rows(dO, Q, K, V, O, LSE, rows, 0.5, False, w),
+                               tq.reshape(-1, d), rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal,S_q,S_k", [(True, 6, 9), (False, 6, 9), (True, 9, 6), (False, 9, 6)])
+def test_window_one_is_diagonal(causal, S_q, S_k):
+    """w = 1: query i sees only key p_i = i + S_k - S_q (if it exists), so O_i = V_{p_i},
+    LSE_i = scale <Q_i, K_{p_i}>, P = 1, dS = 0 (dQ = dK = 0) and dV_j sums dO_i over the
+    group rows with p_i = j; rows with p_i < 0 see nothing."""
+    rng = np.random.default_rng(26)
+    B, H, H_kv, d = 1, 4, 2, 4
+    g = H // H_kv
+    Q, dO = _rand(rng, B, H, S_q, d), _rand(rng, B, H, S_q, d)
+    K, V = _rand(rng, B, H_kv, S_k, d), _rand(rng, B, H_kv, S_k, d)
+    O, LSE = oracle.ref_fwd(Q, K, V, 0.5, causal, 1)
+    dQ, dK, dV, _ = oracle.ref_bwd(dO, Q, K, V, O, LSE, 0.5, causal, 1)
+    expect_dV = np.zeros_like(V)
+    for h in range(H):
+        for i in range(S_q):
+            p = i + S_k - S_q
+            if p < 0:
+                assert np.isneginf(LSE[0, h, i]) and np.all(O[0, h, i] == 0)
+                continue
+            np.testing.assert_allclose(O[0, h, i], V[0, h // g, p], atol=1e-15)
+            np.testing.assert_allclose(LSE[0, h, i], 0.5 * Q[0, h, i] @ K[0, h // g, p], atol=1e-14)
+            expect_dV[0, h // g, p] += dO[0, h, i]
+    assert np.max(np.abs(dQ)) < 1e-14 and np.max(np.abs(dK)) < 1e-14
+    np.testing.assert_allclose(dV, expect_dV, rtol=1e-14, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_window_wider_than_problem_is_no_window(causal):
+    rng = np.random.default_rng(27)
+    B, H, H_kv, S_q, S_k, d = 1, 2, 1, 7, 10, 4
+    Q, dO = _rand(rng, B, H, S_q, d), _rand(rng, B, H, S_q, d)
+    K, V = _rand(rng, B, H_kv, S_k, d), _rand(rng, B, H_kv, S_k, d)
+    O0, L0 = oracle.ref_fwd(Q, K, V, 0.5, causal)
+    Ow, Lw = oracle.ref_fwd(Q, K, V, 0.5, causal, S_q + S_k)
+    assert np.array_equal(O0, Ow) and np.array_equal(L0, Lw)
+    for a, b in zip(oracle.ref_bwd(dO, Q, K, V, O0, L0, 0.5, causal),
+                    oracle.ref_bwd(dO, Q, K, V, Ow, Lw, 0.5, causal, S_q + S_k)):
+        assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 1, 6, 6, 4, True, 2), (1, 2, 2, 5, 7, 4, False, 3)])
+def test_window_matches_finite_differences(shape):
+    B, H, H_kv, S_q, S_k, d, causal, w = shape
+    rng = np.random.default_rng(28)
+    Q, K, V = _rand(rng, B, H, S_q, d), _rand(rng, B, H_kv, S_k, d), _rand(rng, B, H_kv, S_k, d)
+    dO = _rand(rng, B, H, S_q, d)
+    O, LSE = oracle.ref_fwd(Q, K, V, 0.5, causal, w)
+    grads = oracle.ref_bwd(dO, Q, K, V, O, LSE, 0.5, causal, w)[:3]
+    eps = 1e-5
+    for which, (X, G) in enumerate(zip((Q, K, V), grads)):
+        fd = np.zeros_like(X)
+        for idx in itertools.product(*map(range, X.shape)):
+            args = [Q.copy(), K.copy(), V.copy()]
+            args[which][idx] += eps
+            lp = float(np.sum(dO * oracle.ref_fwd(*args, 0.5, causal, w)[0]))
+            args[which][idx] -= 2 * eps
+            lm = float(np.sum(dO * oracle.ref_fwd(*args, 0.5, causal, w)[0]))
+            fd[idx] = (lp - lm) / (2 * eps)
+        err = np.max(np.abs(fd - G)) / max(np.max(np.abs(G)), 1e-30)
+        assert err < 1e-7, (which, err)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_window_sampled_rows_match_full_backward(causal):
+    rng = np.random.default_rng(29)
+    B, H, H_kv, S_q, S_k, d, w = 1, 4, 2, 19, 23, 8, 5
+    Q, K, V = _rand(rng, B, H, S_q, d), _rand(rng, B, H_kv, S_k, d), _rand(rng, B, H_kv, S_k, d)
+    dO = _rand(rng, B, H, S_q, d)
+    O, LSE = oracle.ref_fwd(Q, K, V, 0.3, causal, w)
+    dQ, dK, dV, _ = oracle.ref_bwd(dO, Q, K, V, O, LSE, 0.3, causal, w)
+    qrows = np.array([0, 4, S_q - 1, S_q + 2, B * H * S_q - 1])
+    krows = np.array([0, 3, 9, S_k - 1, S_k + 10, B * H_kv * S_k - 1])
+    np.testing.assert_allclose(oracle.ref_dq_rows(dO, Q, K, V, O, LSE, qrows, 0.3, causal, w),
+                               dQ.reshape(-1, d)[qrows], rtol=1e-13, atol=1e-14)
+    dk, dv = oracle.ref_dkv_rows(dO, Q, K, V, O, LSE, krows, 0.3, causal, w)
+    np.testing.assert_allclose(dk, dK.reshape(-1, d)[krows], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(dv, dV.reshape(-1, d)[krows], rtol=1e-13, atol=1e-14)
