@@ -169,7 +169,7 @@ def main_kernel_traffic(workload: str):
 
 def workload_config(w, extra=None):
     cfg = {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.H_kv, "S_q": w.S_q, "S_k": w.S_k,
-           "d": w.d, "causal": w.causal, "scale": "1/sqrt(d)", "dtype": w.dtype,
+           "d": w.d, "causal": w.causal, "window": w.window, "scale": "1/sqrt(d)", "dtype": w.dtype,
            "inputs": f"Q,K,V~N(0,1), dO~N(0,{w.do_std}^2), seed {w.seed}; O, LSE from the library forward"}
     if extra:
         cfg.update(extra)
@@ -179,9 +179,10 @@ def workload_config(w, extra=None):
 def cpu_oracle_time(w, Q, K, V, dO, O, LSE, batches: int):
     """fp64 oracle backward on the first `batches` batch entries (all heads, full sequences)."""
     import oracle
+    batches = min(batches, w.B)
     args = [x[:batches].detach().to("cpu", torch.float64).numpy() for x in (dO, Q, K, V, O, LSE)]
     t0 = time.perf_counter()
-    oracle.ref_bwd(*args, w.scale, w.causal)
+    oracle.ref_bwd(*args, w.scale, w.causal, w.window)
     dt = time.perf_counter() - t0
     flops = w.with_(B=batches).flops()
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
@@ -195,22 +196,22 @@ def run_reference(args, world, rank):
     if rank != 0:
         return 0
     import oracle
-    w = WORKLOADS[BENCH_WORKLOAD]
+    w = WORKLOADS[args.workload]
     sample_b = 1
     ws = w.with_(B=sample_b)
     if args.ref_seq:  # a shorter sample of the same heads and head dim (quick checks)
         ws = ws.with_(S_q=min(args.ref_seq, w.S_q), S_k=min(args.ref_seq, w.S_k))
     Q, K, V, dO = make_inputs(ws)
     args64 = [x.to(torch.float64).numpy() for x in (Q, K, V, dO)]
-    O, LSE = oracle.ref_fwd(args64[0], args64[1], args64[2], w.scale, w.causal)
+    O, LSE = oracle.ref_fwd(args64[0], args64[1], args64[2], w.scale, w.causal, w.window)
     bwd_args = (args64[3], args64[0], args64[1], args64[2], O, LSE)
     for _ in range(args.warmup):
-        oracle.ref_bwd(*bwd_args, w.scale, w.causal)
+        oracle.ref_bwd(*bwd_args, w.scale, w.causal, w.window)
     times = []
     t_all = time.perf_counter()
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle.ref_bwd(*bwd_args, w.scale, w.causal)
+        oracle.ref_bwd(*bwd_args, w.scale, w.causal, w.window)
         times.append(time.perf_counter() - t0)
     total = time.perf_counter() - t_all
     ms = 1e3 * statistics.mean(times)
@@ -231,9 +232,10 @@ def run_reference(args, world, rank):
 
 def run_forward(args, fa, w, Q, K, V, O, LSE, flush, stream, world, rank, device):
     """The forward (O and LSE the backward consumes) on the bench workload: CUDA events per
-    call, L2 flushed between calls; 4·B·H·S_q·S_k·d flops, halved for causal."""
+    call, L2 flushed between calls; 4·B·H·S_q·S_k·d flops, halved for causal (the band's
+    pairs with a sliding window)."""
     for _ in range(args.warmup):
-        fa.fa_fwd(Q, K, V, scale=w.scale, causal=w.causal, O=O, LSE=LSE)
+        fa.fa_fwd(Q, K, V, scale=w.scale, causal=w.causal, O=O, LSE=LSE, window_size=w.window)
     torch.cuda.synchronize(device)
     fa.fa_check_device()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -242,12 +244,12 @@ def run_forward(args, fa, w, Q, K, V, O, LSE, flush, stream, world, rank, device
     for i in range(args.steps):
         flush.zero_()
         starts[i].record(stream)
-        fa.fa_fwd(Q, K, V, scale=w.scale, causal=w.causal, O=O, LSE=LSE)
+        fa.fa_fwd(Q, K, V, scale=w.scale, causal=w.causal, O=O, LSE=LSE, window_size=w.window)
         ends[i].record(stream)
     torch.cuda.synchronize(device)
     fa.fa_check_device()
     ms = max_over_ranks(statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends)), world, device)
-    flops = 4.0 * w.B * w.H * w.S_q * w.S_k * w.d * (0.5 if w.causal else 1.0)
+    flops = w.fwd_flops()
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     value = world * flops / (ms / 1e3) / 1e12
@@ -258,8 +260,26 @@ def run_forward(args, fa, w, Q, K, V, O, LSE, flush, stream, world, rank, device
                           "roofline": {"bound": "tensor", "achieved": value / world, "peak": peak,
                                        "unit": "TFLOP/s", "frac": value / world / peak,
                                        "peak_source": f"{peak_src} bf16_tflops (burst)"},
-                          "config": {"workload": w.name, "l2": "flushed between calls (256 MiB write)"}}),
+                          "config": workload_config(w, {"l2": "flushed between calls (256 MiB write)"})}),
               flush=True)
+
+
+def run_e2e(args, fa, w, dO, Q, K, V, O, LSE, flops, world, device):
+    """The same backward through fa_bwd_host: pinned host inputs in, host results out,
+    every copy inside the timed region."""
+    host_in = [x.detach().cpu().pin_memory() for x in (dO, Q, K, V, O, LSE)]
+    host_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (Q, K, V)]
+    fa.fa_bwd_host(*host_in, scale=w.scale, causal=w.causal, dQ=host_out[0], dK=host_out[1], dV=host_out[2])
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        fa.fa_bwd_host(*host_in, scale=w.scale, causal=w.causal, dQ=host_out[0], dK=host_out[1],
+                       dV=host_out[2])
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / args.e2e_steps, world, device)
+    h2d = sum(x.numel() * x.element_size() for x in host_in)
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
+    return {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3, "steps": args.e2e_steps}
 
 
 def main():
@@ -276,6 +296,8 @@ def main():
                     help="reference arm: limit the sampled sequence length (0 = the workload's)")
     ap.add_argument("--forward", action="store_true",
                     help="time the forward (fa_fwd) on the same workload instead of the backward")
+    ap.add_argument("--workload", default=BENCH_WORKLOAD, choices=sorted(WORKLOADS),
+                    help="workload to time (default: the headline one)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -289,10 +311,10 @@ def main():
         raise SystemExit("bench.py needs a CUDA device")
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    w = WORKLOADS[BENCH_WORKLOAD]
+    w = WORKLOADS[args.workload]
     Qh, Kh, Vh, dOh = make_inputs(w)
     Q, K, V, dO = (x.to(device) for x in (Qh, Kh, Vh, dOh))
-    O, LSE = fa.fa_fwd(Q, K, V, scale=w.scale, causal=w.causal)
+    O, LSE = fa.fa_fwd(Q, K, V, scale=w.scale, causal=w.causal, window_size=w.window)
     dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
@@ -300,7 +322,8 @@ def main():
         return run_forward(args, fa, w, Q, K, V, O, LSE, flush, stream, world, rank, device)
 
     for _ in range(args.warmup):
-        fa.fa_bwd(dO, Q, K, V, O, LSE, scale=w.scale, causal=w.causal, dQ=dQ, dK=dK, dV=dV)
+        fa.fa_bwd(dO, Q, K, V, O, LSE, scale=w.scale, causal=w.causal, dQ=dQ, dK=dK, dV=dV,
+                  window_size=w.window)
     torch.cuda.synchronize(device)
     fa.fa_check_device()
 
@@ -316,7 +339,8 @@ def main():
     for i in range(args.steps):
         flush.zero_()
         starts[i].record(stream)
-        fa.fa_bwd(dO, Q, K, V, O, LSE, scale=w.scale, causal=w.causal, dQ=dQ, dK=dK, dV=dV)
+        fa.fa_bwd(dO, Q, K, V, O, LSE, scale=w.scale, causal=w.causal, dQ=dQ, dK=dK, dV=dV,
+                  window_size=w.window)
         ends[i].record(stream)
     torch.cuda.synchronize(device)
     barrier(world)
@@ -339,25 +363,15 @@ def main():
     traffic = main_kernel_traffic(w.name)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic, "peak_source": f"{peak_src} bf16_tflops (burst)",
-                "kernel": "bwd_sm103_kernel<bf16,128>", "kernel_ms": main_ms,
+                "kernel": f"bwd_sm103_kernel<{w.dtype},{w.d}>", "kernel_ms": main_ms,
                 "preprocess_ms": ms_pre / max(calls, 1), "finalize_ms": ms_fin / max(calls, 1),
                 "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", 1700.0)),
                 "step_frac": (flops / (ms / 1e3) / 1e12) / peak}
 
-    # ---- end to end through the host-buffer entry point
-    host_in = [x.detach().cpu().pin_memory() for x in (dO, Q, K, V, O, LSE)]
-    host_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (Q, K, V)]
-    fa.fa_bwd_host(*host_in, scale=w.scale, causal=w.causal, dQ=host_out[0], dK=host_out[1], dV=host_out[2])
-    barrier(world)
-    t0 = time.perf_counter()
-    for _ in range(args.e2e_steps):
-        fa.fa_bwd_host(*host_in, scale=w.scale, causal=w.causal, dQ=host_out[0], dK=host_out[1],
-                       dV=host_out[2])
-    e2e_s = max_over_ranks((time.perf_counter() - t0) / args.e2e_steps, world, device)
-    h2d = sum(x.numel() * x.element_size() for x in host_in)
-    d2h = sum(x.numel() * x.element_size() for x in host_out)
-    e2e = {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3, "steps": args.e2e_steps}
+    # ---- end to end through the host-buffer entry point (no sliding window there)
+    e2e = None
+    if w.window == 0:
+        e2e = run_e2e(args, fa, w, dO, Q, K, V, O, LSE, flops, world, device)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -367,7 +381,7 @@ def main():
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
                 "data": "synthetic (seeded normal inputs of the workload's shapes)",
                 "config": workload_config(w, {"l2": "flushed between steps (256 MiB write, outside the events)",
                                               "parallelism": "replicas" if world > 1 else "single GPU"}),

@@ -27,7 +27,8 @@ _lock = threading.Lock()
 _lib = None
 
 #: every symbol include/fa.h declares
-EXPORTS = ("fa_bwd", "fa_bwd_noalloc", "fa_bwd_preprocess", "fa_fwd", "fa_bwd_host", "fa_bwd_workspace_bytes",
+EXPORTS = ("fa_bwd", "fa_bwd_ex", "fa_bwd_noalloc", "fa_bwd_preprocess", "fa_fwd", "fa_fwd_ex", "fa_bwd_host",
+           "fa_bwd_workspace_bytes",
            "fa_check_device", "fa_profile", "fa_profile_read", "fa_selftest_timeout",
            "fa_last_error", "fa_shutdown", "fa_version")
 
@@ -64,6 +65,10 @@ def load_library(path: str | None = None):
         lib.fa_bwd_preprocess.restype = I
         lib.fa_fwd.argtypes = [V, V, V, V, V, I, I, I, I, I, I, F, I, I, V]
         lib.fa_fwd.restype = I
+        lib.fa_bwd_ex.argtypes = [V] * 9 + [I] * 6 + [F, I, I, I, I, V]
+        lib.fa_bwd_ex.restype = I
+        lib.fa_fwd_ex.argtypes = [V, V, V, V, V, I, I, I, I, I, I, F, I, I, I, V]
+        lib.fa_fwd_ex.restype = I
         lib.fa_bwd_workspace_bytes.argtypes = [I, I, I, I]
         lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_check_device.argtypes = [V]
@@ -151,8 +156,9 @@ def _dims(Q, K):
 
 
 def fa_bwd(dO, Q, K, V, O, LSE, scale: float | None = None, causal: bool = False,
-           dQ=None, dK=None, dV=None, stream=None):
-    """dQ, dK, dV of attention; see include/fa.h (fa_bwd)."""
+           dQ=None, dK=None, dV=None, stream=None, window_size: int = 0, deterministic: bool = False):
+    """dQ, dK, dV of attention; see include/fa.h (fa_bwd, and fa_bwd_ex when a
+    sliding window or the deterministic mode is asked for)."""
     B, H, H_kv, S_q, S_k, d = _dims(Q, K)
     for name, t, shp in (("dO", dO, Q.shape), ("O", O, Q.shape), ("V", V, K.shape)):
         if tuple(t.shape) != tuple(shp):
@@ -167,10 +173,15 @@ def fa_bwd(dO, Q, K, V, O, LSE, scale: float | None = None, causal: bool = False
     for name, t, ref in (("dQ", dQ, Q), ("dK", dK, K), ("dV", dV, V)):
         if t.shape != ref.shape or t.dtype != ref.dtype or not t.is_contiguous():
             raise FaError(1, f"{name}: must be contiguous {ref.dtype} {tuple(ref.shape)}")
+    lib = load_library()
+    args = (_ptr(dO), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _ptr(dQ), _ptr(dK), _ptr(dV),
+            B, H, H_kv, S_q, S_k, d, scale, int(bool(causal)))
     with torch.cuda.device(dev):
-        _check(load_library().fa_bwd(_ptr(dO), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE),
-                                     _ptr(dQ), _ptr(dK), _ptr(dV), B, H, H_kv, S_q, S_k, d, scale,
-                                     int(bool(causal)), _dtype(Q), _stream(stream)))
+        if int(window_size) == 0 and not deterministic:
+            _check(lib.fa_bwd(*args, _dtype(Q), _stream(stream)))
+        else:
+            _check(lib.fa_bwd_ex(*args, int(window_size), int(bool(deterministic)), _dtype(Q),
+                                 _stream(stream)))
     return dQ, dK, dV
 
 
@@ -219,17 +230,21 @@ def fa_bwd_preprocess(dO, O, D=None, stream=None):
 
 
 def fa_fwd(Q, K, V, scale: float | None = None, causal: bool = False, O=None, LSE=None,
-           stream=None):
-    """(O, LSE) of attention; see include/fa.h (fa_fwd)."""
+           stream=None, window_size: int = 0):
+    """(O, LSE) of attention; see include/fa.h (fa_fwd, fa_fwd_ex for a sliding window)."""
     B, H, H_kv, S_q, S_k, d = _dims(Q, K)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     dev = _on_device((Q, K, V, O, LSE))
     O = torch.empty_like(Q) if O is None else O
     LSE = torch.empty((B, H, S_q), dtype=torch.float32, device=dev) if LSE is None else LSE
+    lib = load_library()
+    args = (_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, H, H_kv, S_q, S_k, d, scale,
+            int(bool(causal)))
     with torch.cuda.device(dev):
-        _check(load_library().fa_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, H, H_kv,
-                                     S_q, S_k, d, scale, int(bool(causal)), _dtype(Q),
-                                     _stream(stream)))
+        if int(window_size) == 0:
+            _check(lib.fa_fwd(*args, _dtype(Q), _stream(stream)))
+        else:
+            _check(lib.fa_fwd_ex(*args, int(window_size), _dtype(Q), _stream(stream)))
     return O, LSE
 
 

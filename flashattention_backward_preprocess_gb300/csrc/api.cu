@@ -136,7 +136,8 @@ int check_ptr(const void* p, const char* name, size_t align) {
     return FA_OK;
 }
 
-Shape make_shape(int B, int H, int H_kv, int S_q, int S_k, int d, float scale, int causal) {
+Shape make_shape(int B, int H, int H_kv, int S_q, int S_k, int d, float scale, int causal,
+                 int window = 0) {
     Shape s;
     s.B = B;
     s.H = H;
@@ -146,6 +147,7 @@ Shape make_shape(int B, int H, int H_kv, int S_q, int S_k, int d, float scale, i
     s.d = d;
     s.scale = scale;
     s.causal = causal ? 1 : 0;
+    s.window = window;
     s.S_q_pad = pad_rows(S_q);
     return s;
 }
@@ -195,18 +197,24 @@ bool fwd_simt_for_16bit() {
     return v == 1;
 }
 
+int check_window(int window) {
+    if (window < 0) return fail(FA_ERR_INVALID_ARG, "window_size", "must be >= 0 (0 = no window)");
+    return FA_OK;
+}
+
 int bwd_impl(const void* dO, const void* Q, const void* K, const void* V, const void* O,
              const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv, int S_q,
-             int S_k, int d, float scale, int causal, int dtype, cudaStream_t st) {
+             int S_k, int d, float scale, int causal, int window, int dtype, cudaStream_t st) {
     int rc;
     if ((rc = check_dims(B, H, H_kv, S_q, S_k, d, dtype))) return rc;
     if ((rc = check_scale(scale))) return rc;
     if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal", "must be 0 or 1");
+    if ((rc = check_window(window))) return rc;
     if ((rc = check_ptr(dO, "dO", 16)) || (rc = check_ptr(Q, "Q", 16)) || (rc = check_ptr(K, "K", 16)) ||
         (rc = check_ptr(V, "V", 16)) || (rc = check_ptr(O, "O", 16)) || (rc = check_ptr(LSE, "LSE", 4)) ||
         (rc = check_ptr(dQ, "dQ", 16)) || (rc = check_ptr(dK, "dK", 16)) || (rc = check_ptr(dV, "dV", 16)))
         return rc;
-    const Shape s = make_shape(B, H, H_kv, S_q, S_k, d, scale, causal);
+    const Shape s = make_shape(B, H, H_kv, S_q, S_k, d, scale, causal, window);
     const WsLayout L = ws_layout(B, H, S_q, d);
     void* base = nullptr;
     if ((rc = get_workspace(st, L.total, &base))) return rc;
@@ -218,8 +226,9 @@ int bwd_impl(const void* dO, const void* Q, const void* K, const void* V, const 
     const bool tc = dtype != FA_F32 && !use_simt_for_16bit();
     if (debug_enabled())
         fprintf(stderr,
-                "[fa] bwd B=%d H=%d H_kv=%d S_q=%d S_k=%d d=%d causal=%d dtype=%d kernel=%s grid=%d ws=%zu\n",
-                B, H, H_kv, S_q, S_k, d, causal, dtype, tc ? "sm103" : "simt",
+                "[fa] bwd B=%d H=%d H_kv=%d S_q=%d S_k=%d d=%d causal=%d window=%d dtype=%d kernel=%s grid=%d "
+                "ws=%zu\n",
+                B, H, H_kv, S_q, S_k, d, causal, window, dtype, tc ? "sm103" : "simt",
                 tc ? (S_k + kTileK - 1) / kTileK * B * H_kv : 0, L.total);
     ProfRec pr;
     const bool prof = prof_begin(&pr);
@@ -237,6 +246,31 @@ int bwd_impl(const void* dO, const void* Q, const void* K, const void* V, const 
         cudaEventRecord(pr.ev[3], st);
         prof_end(pr);
     }
+    return FA_OK;
+}
+
+int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int H_kv,
+             int S_q, int S_k, int d, float scale, int causal, int window, int dtype, cudaStream_t st) {
+    int rc;
+    if ((rc = check_dims(B, H, H_kv, S_q, S_k, d, dtype))) return rc;
+    if ((rc = check_scale(scale))) return rc;
+    if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal", "must be 0 or 1");
+    if ((rc = check_window(window))) return rc;
+    if ((rc = check_ptr(Q, "Q", 16)) || (rc = check_ptr(K, "K", 16)) || (rc = check_ptr(V, "V", 16)) ||
+        (rc = check_ptr(O, "O", 16)) || (rc = check_ptr(LSE, "LSE", 4)))
+        return rc;
+    const Shape s = make_shape(B, H, H_kv, S_q, S_k, d, scale, causal, window);
+    cudaError_t e;
+    if (dtype == FA_F32 || fwd_simt_for_16bit()) {
+        e = launch_fwd_simt(dtype, Q, K, V, O, LSE, s, st);
+    } else {
+        // the tensor-core forward reports bounded-wait timeouts in the stream's workspace
+        // error words (fa_check_device reads them)
+        void* base = nullptr;
+        if ((rc = get_workspace(st, 256, &base))) return rc;
+        e = launch_fwd_sm103(dtype, Q, K, V, O, LSE, static_cast<unsigned int*>(base), s, st);
+    }
+    if (e != cudaSuccess) return cuda_fail("forward launch", e);
     return FA_OK;
 }
 
@@ -286,8 +320,19 @@ int fa_bwd(const void* dO, const void* Q, const void* K, const void* V, const vo
            const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv, int S_q,
            int S_k, int d, float scale, int causal, int dtype, void* stream) {
     g_last_error.clear();
-    return bwd_impl(dO, Q, K, V, O, LSE, dQ, dK, dV, B, H, H_kv, S_q, S_k, d, scale, causal, dtype,
+    return bwd_impl(dO, Q, K, V, O, LSE, dQ, dK, dV, B, H, H_kv, S_q, S_k, d, scale, causal, 0, dtype,
                     static_cast<cudaStream_t>(stream));
+}
+
+int fa_bwd_ex(const void* dO, const void* Q, const void* K, const void* V, const void* O,
+              const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv, int S_q,
+              int S_k, int d, float scale, int causal, int window_size, int deterministic, int dtype,
+              void* stream) {
+    g_last_error.clear();
+    if (deterministic != 0)
+        return fail(FA_ERR_UNSUPPORTED, "deterministic", "only 0 (fp32 atomic dQ reduction) is available");
+    return bwd_impl(dO, Q, K, V, O, LSE, dQ, dK, dV, B, H, H_kv, S_q, S_k, d, scale, causal, window_size,
+                    dtype, static_cast<cudaStream_t>(stream));
 }
 
 int fa_bwd_preprocess(const void* dO, const void* O, float* D, int B, int H, int S_q, int d,
@@ -307,27 +352,16 @@ int fa_bwd_preprocess(const void* dO, const void* O, float* D, int B, int H, int
 int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
            int H_kv, int S_q, int S_k, int d, float scale, int causal, int dtype, void* stream) {
     g_last_error.clear();
-    int rc;
-    if ((rc = check_dims(B, H, H_kv, S_q, S_k, d, dtype))) return rc;
-    if ((rc = check_scale(scale))) return rc;
-    if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal", "must be 0 or 1");
-    if ((rc = check_ptr(Q, "Q", 16)) || (rc = check_ptr(K, "K", 16)) || (rc = check_ptr(V, "V", 16)) ||
-        (rc = check_ptr(O, "O", 16)) || (rc = check_ptr(LSE, "LSE", 4)))
-        return rc;
-    const Shape s = make_shape(B, H, H_kv, S_q, S_k, d, scale, causal);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    if (dtype == FA_F32 || fwd_simt_for_16bit()) {
-        e = launch_fwd_simt(dtype, Q, K, V, O, LSE, s, st);
-    } else {
-        // the tensor-core forward reports bounded-wait timeouts in the stream's workspace
-        // error words (fa_check_device reads them)
-        void* base = nullptr;
-        if ((rc = get_workspace(st, 256, &base))) return rc;
-        e = launch_fwd_sm103(dtype, Q, K, V, O, LSE, static_cast<unsigned int*>(base), s, st);
-    }
-    if (e != cudaSuccess) return cuda_fail("forward launch", e);
-    return FA_OK;
+    return fwd_impl(Q, K, V, O, LSE, B, H, H_kv, S_q, S_k, d, scale, causal, 0, dtype,
+                    static_cast<cudaStream_t>(stream));
+}
+
+int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+              int H_kv, int S_q, int S_k, int d, float scale, int causal, int window_size, int dtype,
+              void* stream) {
+    g_last_error.clear();
+    return fwd_impl(Q, K, V, O, LSE, B, H, H_kv, S_q, S_k, d, scale, causal, window_size, dtype,
+                    static_cast<cudaStream_t>(stream));
 }
 
 int fa_bwd_host(const void* dO, const void* Q, const void* K, const void* V, const void* O,
@@ -420,7 +454,7 @@ int fa_bwd_host(const void* dO, const void* Q, const void* K, const void* V, con
             return cuda_fail("cudaEventRecord / cudaStreamWaitEvent", e);
         auto at = [&](int slot) { return dbase + off[slot] + u0 * unit_bytes(slot); };
         rc = bwd_impl(at(0), at(1), at(4), at(5), at(2), reinterpret_cast<const float*>(at(8)), at(3), at(6), at(7),
-                      1, nu * g, nu, S_q, S_k, d, scale, causal, dtype, st);
+                      1, nu * g, nu, S_q, S_k, d, scale, causal, 0, dtype, st);
         if (rc != FA_OK) return rc;
         if ((e = cudaEventRecord(hs->ev_done[c], st)) != cudaSuccess ||
             (e = cudaStreamWaitEvent(hs->s_out, hs->ev_done[c], 0)) != cudaSuccess)

@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_kernel(
     const int bkv = blockIdx.y;  // b * H_kv + hk
     const int b = bkv / s.H_kv, hk = bkv % s.H_kv;
     const int g = s.H / s.H_kv;
-    const int off = s.S_k - s.S_q;  // causal: key j visible to query i iff j <= i + off
+    const int off = s.S_k - s.S_q;  // query i sits at key position i + off
     const float kLog2e = 1.4426950408889634f;
 
     for (int e = tid; e < kTile * D; e += kThreads) {
@@ -55,13 +55,13 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_kernel(
     }
     __syncthreads();
 
-    // first query row that can see a key of this tile
-    int i_begin = 0;
-    if (s.causal) i_begin = max(0, n0 - off);
+    // query rows [i_begin, i_end) see a key of this tile
+    int i_begin, i_end;
+    query_range(s, n0, min(n0 + kTile, s.S_k), i_begin, i_end);
 
     for (int h = hk * g; h < (hk + 1) * g; ++h) {
         const int bh = b * s.H + h;
-        for (int i = i_begin; i < s.S_q; ++i) {
+        for (int i = i_begin; i < i_end; ++i) {
             const size_t qi = ((size_t)bh * s.S_q + i) * D;
             for (int c = tid; c < D; c += kThreads) {
                 sq[c] = TypeTraits<T>::to_f32(Q[qi + c]);
@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_kernel(
                 }
                 if (lane == 0) {
                     const int jj = n0 + j;
-                    const bool vis = jj < s.S_k && (!s.causal || jj <= i + off);
+                    const bool vis = jj < s.S_k && key_visible(i + off, jj, s.causal, s.window);
                     // exp(scale*S - LSE) = exp2(scale*log2e*S - LSE*log2e)
                     const float p = vis ? exp2f(fmaf(sd, s.scale * kLog2e, -l2)) : 0.f;
                     sp[j] = p;

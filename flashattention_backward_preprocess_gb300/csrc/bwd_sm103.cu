@@ -110,7 +110,7 @@ struct Params {
     unsigned int* err;
     int B, H, H_kv, S_q, S_k, S_q_pad;
     float scale, scale_log2;
-    int causal;
+    int causal, window;
 };
 
 // TMEM column (relative to a buffer) of the packed 16-bit A operand for MMA k-step k
@@ -165,14 +165,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b = bkv / p.H_kv, hk = bkv % p.H_kv;
     const int g = p.H / p.H_kv;
     const int n0 = n_tile * BN;
-    const int off = p.S_k - p.S_q;  // key j visible to query i iff j <= i + off (causal)
-    const int m_tiles = (p.S_q + BM - 1) / BM;
-    int m_start = 0;
-    if (p.causal) {
-        const int first_q = n0 - off;  // first query row that can see key n0
-        m_start = first_q <= 0 ? 0 : first_q / BM;
+    const int off = p.S_k - p.S_q;  // query i sits at key position i + off
+    // query tiles [m_start, m_end) hold every row that sees a key of this tile (causal
+    // edge below, sliding-window band edges on either side)
+    int q_lo, q_hi;
+    {
+        Shape sh;
+        sh.S_q = p.S_q;
+        sh.S_k = p.S_k;
+        sh.causal = p.causal;
+        sh.window = p.window;
+        query_range(sh, n0, min(n0 + BN, p.S_k), q_lo, q_hi);
     }
-    const int nm = m_tiles > m_start ? m_tiles - m_start : 0;
+    const int m_start = q_lo / BM;
+    const int m_end = q_hi > q_lo ? (q_hi + BM - 1) / BM : m_start;
+    const int nm = m_end - m_start;
     const int n_it = g * nm;
 
     if (threadIdx.x == 0) {
@@ -200,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     auto iter_coords = [&](int it, int& bh, int& m0) {
         const int hh = it % g;
-        m0 = (m_tiles - 1 - it / g) * BM;
+        m0 = (m_end - 1 - it / g) * BM;
         bh = b * p.H + hk * g + hh;
     };
 
@@ -341,9 +348,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             int bh, m0;
             iter_coords(it, bh, m0);
             const int i_lo = m0 + qh;  // first query row of this warp's columns
+            // Columns q of this warp (query i_lo + q, key position i_lo + off + q) that see
+            // this lane's key j form one interval (visible_queries); a padding key row sees
+            // nothing.  Only qa stays live across the waits: the bounds are cheap to redo.
+            const int qa = j - i_lo - off;
             // warp-uniform: the chosen path holds .sync.aligned TMEM accesses; the per-element
             // selects inside the masked path handle each lane's own row
-            const bool mask_tile = __any_sync(0xffffffffu, !row_valid || (p.causal && j > i_lo + off));
+            bool full;
+            {
+                int lo, hi;
+                visible_queries(qa, p.causal, p.window, lo, hi);
+                full = row_valid && lo <= 0 && hi >= kHalfQ;
+            }
+            const bool mask_tile = __any_sync(0xffffffffu, !full);
             const float* sl = reinterpret_cast<const float*>(smem + C::OFF_LSE + s * BM * 4) + qh;
             const float* sd = reinterpret_cast<const float*>(smem + C::OFF_DD + s * BM * 4) + qh;
             if (!(ok = wait_bar_warp(bar_full(s), (it / C::STAGES) & 1, abort_flag, p.err))) break;
@@ -369,11 +386,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     a = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
                     b = make_float2(ptx::ex2(b.x), ptx::ex2(b.y));
                     if (masked) {
-                        const int lim = i_lo + q + off;  // key j visible to query i_lo+q+u iff j <= lim+u
-                        a.x = (row_valid && (!p.causal || j <= lim + 0)) ? a.x : 0.f;
-                        a.y = (row_valid && (!p.causal || j <= lim + 1)) ? a.y : 0.f;
-                        b.x = (row_valid && (!p.causal || j <= lim + 2)) ? b.x : 0.f;
-                        b.y = (row_valid && (!p.causal || j <= lim + 3)) ? b.y : 0.f;
+                        int q_lo, q_hi;
+                        visible_queries(qa, p.causal, p.window, q_lo, q_hi);
+                        const unsigned q_span = row_valid ? (unsigned)(q_hi - q_lo) : 0u;
+                        a.x = (unsigned)(q + 0 - q_lo) < q_span ? a.x : 0.f;
+                        a.y = (unsigned)(q + 1 - q_lo) < q_span ? a.y : 0.f;
+                        b.x = (unsigned)(q + 2 - q_lo) < q_span ? b.x : 0.f;
+                        b.y = (unsigned)(q + 3 - q_lo) < q_span ? b.y : 0.f;
                     }
                     Pp[q / 2] = pack2<kBF16>(a.x, a.y);
                     Pp[q / 2 + 1] = pack2<kBF16>(b.x, b.y);
@@ -605,6 +624,7 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, const void* dO
     p.scale = s.scale;
     p.scale_log2 = s.scale * 1.4426950408889634f;
     p.causal = s.causal;
+    p.window = s.window;
     auto kern = bwd_sm103_kernel<T, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;

@@ -35,8 +35,63 @@ struct Shape {
     int B, H, H_kv, S_q, S_k, d;
     float scale;
     int causal;
+    int window;   // sliding-window size, 0 = none
     int S_q_pad;  // S_q rounded up to the main kernel's query tile (128)
 };
+
+// Visibility of key j to query i.  Query i sits at key position p = i + S_k - S_q
+// (bottom-right alignment).  Causal hides keys after p.  A sliding window w > 0
+// (boostr autograd_attention.rs, window_size of FlashAttentionConfig; 0 = none)
+// hides keys w or more positions before p and, when not causal, w or more after.
+__host__ __device__ __forceinline__ bool key_visible(int p, int j, int causal, int window) {
+    if (causal && j > p) return false;
+    if (window > 0 && (p - j >= window || (!causal && j - p >= window))) return false;
+    return true;
+}
+
+// The same test for a run of positions, as one interval (kernels compare each element
+// against it with a single unsigned comparison; kOpen stands for "no bound").
+constexpr int kOpen = 1 << 29;
+
+// Offsets q whose query (key position base + q) sees key j = base + dj: q in [lo, hi).
+__host__ __device__ __forceinline__ void visible_queries(int dj, int causal, int window, int& lo, int& hi) {
+    lo = causal ? dj : (window > 0 ? dj - window + 1 : -kOpen);
+    hi = window > 0 ? dj + window : kOpen;
+}
+
+// Offsets c whose key (base + c) the query at key position base + dp sees: c in [lo, hi).
+__host__ __device__ __forceinline__ void visible_keys(int dp, int causal, int window, int& lo, int& hi) {
+    lo = window > 0 ? dp - window + 1 : -kOpen;
+    hi = causal ? dp + 1 : (window > 0 ? dp + window : kOpen);
+}
+
+// Query rows [lo, hi) that see at least one key of [j0, j1) (j0 < j1 <= S_k);
+// empty when hi <= lo.  Exact for a band: the first such row sees key j0 or is
+// the first past the causal edge, the last one sees key j1 - 1.
+__host__ __device__ __forceinline__ void query_range(const Shape& s, int j0, int j1, int& lo, int& hi) {
+    const int off = s.S_k - s.S_q;
+    lo = 0;
+    hi = s.S_q;
+    if (s.causal) lo = j0 - off > lo ? j0 - off : lo;  // p >= j0
+    if (s.window > 0) {
+        const int h = j1 - 1 + s.window - off;  // p - (j1 - 1) < w
+        hi = h < hi ? h : hi;
+        if (!s.causal) lo = j0 - s.window + 1 - off > lo ? j0 - s.window + 1 - off : lo;  // j0 - p < w
+    }
+}
+
+// Key columns [lo, hi) visible to at least one query row of [i0, i1) (i0 < i1 <= S_q);
+// empty when hi <= lo.
+__host__ __device__ __forceinline__ void key_range(const Shape& s, int i0, int i1, int& lo, int& hi) {
+    const int off = s.S_k - s.S_q;
+    lo = 0;
+    hi = s.S_k;
+    if (s.causal) hi = i1 + off < hi ? i1 + off : hi;  // j <= p of the last row
+    if (s.window > 0) {
+        lo = i0 + off - s.window + 1 > lo ? i0 + off - s.window + 1 : lo;  // p_first - j < w
+        if (!s.causal) hi = i1 - 1 + off + s.window < hi ? i1 - 1 + off + s.window : hi;  // j - p_last < w
+    }
+}
 
 // Device error word codes (bit set by a kernel whose bounded wait ran out).
 enum : unsigned int {

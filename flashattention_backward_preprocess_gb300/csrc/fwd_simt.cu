@@ -54,9 +54,10 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(const T* __restrict_
         for (int cc = 0; cc < CPT; ++cc) acc[a][cc] = 0.f;
     }
 
-    int n_end = s.S_k;
-    if (s.causal) n_end = min(s.S_k, m0 + BM + off);  // keys beyond the tile's last query
-    for (int n0 = 0; n0 < n_end; n0 += BN) {
+    // key columns [n_lo, n_end) hold every key a row of this tile sees
+    int n_lo, n_end;
+    key_range(s, m0, min(m0 + BM, s.S_q), n_lo, n_end);
+    for (int n0 = n_lo - n_lo % BN; n0 < n_end; n0 += BN) {
         __syncthreads();
         for (int e = tid; e < BN * D; e += kThreads) {
             const int r = e / D, c = e % D;
@@ -88,7 +89,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(const T* __restrict_
 #pragma unroll
             for (int bb = 0; bb < 4; ++bb) {
                 const int j = n0 + tx * 4 + bb;
-                const bool vis = j < s.S_k && (!s.causal || j <= i + off);
+                const bool vis = j < s.S_k && key_visible(i + off, j, s.causal, s.window);
                 sc[a][bb] = vis ? sc[a][bb] * s.scale : -INFINITY;
                 rmax = fmaxf(rmax, sc[a][bb]);
             }

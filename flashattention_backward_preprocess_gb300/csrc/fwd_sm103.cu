@@ -2,7 +2,8 @@
 // or 128: the O and LSE the backward consumes (boostr autograd_attention.rs: the
 // forward saves q, k, v, output and lse for FlashAttentionBackward).
 //
-//   s_ij = scale <Q_i, K_j> over the visible keys j (causal: j <= i + S_k - S_q)
+//   s_ij = scale <Q_i, K_j> over the visible keys j (key_visible: causal keeps
+//          j <= i + S_k - S_q, a sliding window a band around that position)
 //   O_i  = sum_j exp(s_ij) V_j / sum_j exp(s_ij),   LSE_i = log sum_j exp(s_ij)
 // computed with the online softmax over 128-key tiles; a row that sees no key
 // gets O = 0 and LSE = -inf.
@@ -67,6 +68,7 @@ struct FParams {
     unsigned int* err;
     int B, H, H_kv, S_q, S_k;
     float scale_log2;
+    int window;  // sliding-window size, 0 = none
 };
 
 template <bool kBF16>
@@ -105,11 +107,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b = bh / p.H, h = bh % p.H;
     const int bkv = b * p.H_kv + h / (p.H / p.H_kv);
     const int m0 = mt * BM;
-    const int off = p.S_k - p.S_q;  // key j visible to query i iff j <= i + off (causal)
-    int n_end = n_tiles;
-    if (causal) {
-        const int last = m0 + BM - 1 + off;  // last key the tile's last row can see
-        n_end = last < 0 ? 0 : (last / BN + 1 < n_tiles ? last / BN + 1 : n_tiles);
+    const int off = p.S_k - p.S_q;  // query i sits at key position i + off
+    // key tiles [n_first, n_first + n_cnt) hold every key a row of this tile sees
+    int n_first = 0, n_cnt = 0;
+    {
+        Shape sh;
+        sh.S_q = p.S_q;
+        sh.S_k = p.S_k;
+        sh.causal = causal;
+        sh.window = p.window;
+        int k_lo, k_hi;
+        key_range(sh, m0, min(m0 + BM, p.S_q), k_lo, k_hi);
+        if (k_hi > k_lo) {
+            n_first = k_lo / BN;
+            n_cnt = min((k_hi + BN - 1) / BN, n_tiles) - n_first;
+        }
     }
 
     if (threadIdx.x == 0) {
@@ -130,19 +142,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kWarpTma) {
         // ------------------------------------------------------------ producer
-        if (lane == 0 && !*abort_flag && n_end > 0) {
+        if (lane == 0 && !*abort_flag && n_cnt > 0) {
             ptx::mbar_arrive_expect_tx(bar(F_Q), C::kTile_B);
             for (int x = 0; x < C::BOXES; ++x)
                 ptx::tma_load_3d(sbase + C::OFF_Q + x * C::kBox_B, &tmQ, x * 64, m0, bh, bar(F_Q));
             int issued = 0;
-            for (int j = 0; j < n_end; ++j) {
+            for (int j = 0; j < n_cnt; ++j) {
                 const int s = j % C::STAGES;
                 if (j >= C::STAGES && !wait_bar(bar_empty(s), ((j / C::STAGES) - 1) & 1, abort_flag, p.err)) break;
                 ptx::mbar_arrive_expect_tx(bar_full(s), 2 * C::kTile_B);
                 for (int x = 0; x < C::BOXES; ++x) {
-                    ptx::tma_load_3d(sbase + C::OFF_K + s * C::kTile_B + x * C::kBox_B, &tmK, x * 64, j * BN, bkv,
+                    ptx::tma_load_3d(sbase + C::OFF_K + s * C::kTile_B + x * C::kBox_B, &tmK, x * 64,
+                                     (n_first + j) * BN, bkv,
                                      bar_full(s));
-                    ptx::tma_load_3d(sbase + C::OFF_V + s * C::kTile_B + x * C::kBox_B, &tmV, x * 64, j * BN, bkv,
+                    ptx::tma_load_3d(sbase + C::OFF_V + s * C::kTile_B + x * C::kBox_B, &tmV, x * 64,
+                                     (n_first + j) * BN, bkv,
                                      bar_full(s));
                 }
                 issued = j + 1;
@@ -154,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && !*abort_flag && n_end > 0) {
+        if (lane == 0 && !*abort_flag && n_cnt > 0) {
             constexpr uint32_t ID_S = ptx::idesc_f16(BM, BN, kBF16, false, false);  // S = Q K^T
             constexpr uint32_t ID_PV = ptx::idesc_f16(BM, D, kBF16, false, true);   // O += P V (A in TMEM)
             auto desc_add = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
@@ -173,12 +187,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mma_commit(bar(F_S0 + (j & 1)));
             };
             bool ok = wait_bar(bar(F_Q), 0, abort_flag, p.err);
-            for (int j = 0; ok && j < 2 && j < n_end; ++j) {
+            for (int j = 0; ok && j < 2 && j < n_cnt; ++j) {
                 if (!(ok = wait_bar(bar_full(j % C::STAGES), (j / C::STAGES) & 1, abort_flag, p.err))) break;
                 ptx::tc_fence_after();
                 gemm_s(j);
             }
-            for (int j = 0; ok && j < n_end; ++j) {
+            for (int j = 0; ok && j < n_cnt; ++j) {
                 const int s = j % C::STAGES;
                 // O += P(j) V(j)   (A = P packed in buffer j % 2: 16 keys = 8 packed columns per step)
                 if (!(ok = wait_bar(bar(F_P0 + (j & 1)), (j >> 1) & 1, abort_flag, p.err))) break;
@@ -189,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 desc_add(dV_mn, (uint32_t)s * C::kTile_B + k * 2048), ID_PV, (j > 0 || k > 0) ? 1u : 0u);
                 ptx::mma_commit(bar(F_PV));
                 ptx::mma_commit(bar_empty(s));  // K(j), V(j) no longer read
-                if (j + 2 < n_end) {
+                if (j + 2 < n_cnt) {
                     // S(j+2) into buffer j % 2 once the P V product has read P(j) out of it
                     const int s2 = (j + 2) % C::STAGES;
                     if (!(ok = wait_bar(bar_full(s2), ((j + 2) / C::STAGES) & 1, abort_flag, p.err))) break;
@@ -212,11 +226,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_run = -INFINITY;  // running max of x = s * log2(e), moved lazily
         float l_run = 0.f;        // sum of exp2(x - m_run)
         bool ok = !*abort_flag;
-        for (int j = 0; ok && j < n_end; ++j) {
+        for (int j = 0; ok && j < n_cnt; ++j) {
             const uint32_t buf = tmem + C::TM_S + (j & 1) * 128 + lane_off;
-            const int n0 = j * BN;
+            const int n0 = (n_first + j) * BN;
+            // Key columns c of this tile (key n0 + c) that the row sees form one interval
+            // (visible_keys of the row's key position i + off), cut to the keys that exist.
+            int c_lo, c_hi;
+            visible_keys(i + off - n0, causal, p.window, c_lo, c_hi);
+            c_lo = max(c_lo, 0);
+            c_hi = min(c_hi, p.S_k - n0);
+            const unsigned c_span = c_hi > c_lo ? (unsigned)(c_hi - c_lo) : 0u;
             // warp-uniform: the chosen path holds .sync.aligned TMEM accesses
-            const bool masked = __any_sync(0xffffffffu, n0 + BN > p.S_k || (causal && n0 + BN - 1 > i + off));
+            const bool masked = __any_sync(0xffffffffu, !(c_lo <= 0 && c_hi >= BN));
             if (!(ok = wait_bar_warp(bar(F_S0 + (j & 1)), (j >> 1) & 1, abort_flag, p.err))) break;
             ptx::tc_fence_after();
             uint32_t r[BN];
@@ -226,11 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             float x[BN];
             float mx = -INFINITY;
             if (masked) {
-                const int lim = causal ? i + off - n0 : BN;  // column c visible iff c <= lim (causal)
-                const int kend = p.S_k - n0;                 // and c < kend
 #pragma unroll
                 for (int c = 0; c < BN; ++c) {
-                    x[c] = (c < kend && c <= lim) ? __uint_as_float(r[c]) * p.scale_log2 : -INFINITY;
+                    x[c] = (unsigned)(c - c_lo) < c_span ? __uint_as_float(r[c]) * p.scale_log2 : -INFINITY;
                     mx = fmaxf(mx, x[c]);
                 }
             } else {
@@ -278,8 +297,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(F_P0 + (j & 1)));
         }
-        // ---- epilogue: O = acc / l, LSE = (m + log2 l) * ln 2
-        if (ok && n_end > 0) ok = wait_bar_warp(bar(F_PV), (n_end - 1) & 1, abort_flag, p.err);
+        // ---- epilogue: O = acc / l, LSE = (m + log2 l) * ln 2.  Wait for the MMA issuer's
+        // final commit (every product done), not for a parity of the shared P V barrier:
+        // after the last tile that barrier may still be in the phase of the product before
+        // last, whose parity is the opposite one, and a parity wait would pass at once.
+        if (ok && n_cnt > 0) ok = wait_bar_warp(bar(F_FINAL), 0, abort_flag, p.err);
         if (ok) {
             ptx::tc_fence_after();
             const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -287,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
-                if (n_end > 0) {
+                if (n_cnt > 0) {
                     ptx::tmem_ld32p(tmem + C::TM_O + lane_off + c * 32, o);
                     ptx::tmem_wait_ld();
                 } else {
@@ -372,6 +394,7 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, void* O, float
     p.S_q = s.S_q;
     p.S_k = s.S_k;
     p.scale_log2 = s.scale * 1.4426950408889634f;
+    p.window = s.window;
     auto kern = fwd_sm103_kernel<T, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;

@@ -110,6 +110,7 @@ extern "C" int fa_bwd_noalloc(const void* dO, const void* Q, const void* K, cons
     s.d = d;
     s.scale = scale;
     s.causal = causal;
+    s.window = 0;
     s.S_q_pad = S_q_pad;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // the preprocess pass also zeroes the dQ accumulator rows this call uses

@@ -14,6 +14,9 @@ this library is measured on):
   bf16_b4_h32_kv8_s2048_d128_causal bf16   4 32   8    2048  2048 128   yes     0.1
   fp16_b1_h16_s8192_d128            f16    1 16  16    8192  8192 128   no      1
   bf16_b8_h16_kv2_sq512_sk4096_d64  bf16   8 16   2     512  4096  64   no      1
+  bf16_b1_h32_kv8_s16384_d128_causal_w4096
+                                    bf16   1 32   8   16384 16384 128   yes     1
+                                    (sliding window of 4096 keys)
 
 scale = 1/sqrt(d) everywhere.
 """
@@ -39,6 +42,7 @@ class Workload:
     causal: bool
     do_std: float = 1.0
     seed: int = 1234
+    window: int = 0     # sliding-window size, 0 = none
 
     @property
     def scale(self) -> float:
@@ -52,10 +56,26 @@ class Workload:
     def elem_bytes(self) -> int:
         return 4 if self.dtype == "f32" else 2
 
+    def pairs(self) -> float:
+        """(query, key) pairs per head the flop counts use: S_q * S_k, halved if causal
+        (the usual causal-adjusted count); with a sliding window, the pairs of the band
+        (a causal query at key position p keeps keys p-w+1..p, a non-causal one
+        p-w+1..p+w-1, clipped to the keys that exist)."""
+        if self.window <= 0:
+            n = float(self.S_q) * self.S_k
+            return n * 0.5 if self.causal else n
+        p = np.arange(self.S_q, dtype=np.int64) + (self.S_k - self.S_q)
+        lo = np.maximum(p - self.window + 1, 0)
+        hi = np.minimum(p + 1 if self.causal else p + self.window, self.S_k)
+        return float(np.maximum(hi - lo, 0).sum())
+
     def flops(self) -> float:
-        """Five S_q x S_k x d GEMMs of the backward (2 flops per MAC), halved if causal."""
-        f = 10.0 * self.B * self.H * self.S_q * self.S_k * self.d
-        return f * 0.5 if self.causal else f
+        """Five S_q x S_k x d GEMMs of the backward (2 flops per MAC) over pairs()."""
+        return 10.0 * self.B * self.H * self.pairs() * self.d
+
+    def fwd_flops(self) -> float:
+        """Two GEMMs of the forward (2 flops per MAC) over pairs()."""
+        return 4.0 * self.B * self.H * self.pairs() * self.d
 
     def algorithmic_bytes(self) -> int:
         """Read Q, K, V, O, dO, LSE; D written and read once; write dQ, dK, dV."""
@@ -78,6 +98,8 @@ WORKLOADS = {
         Workload("fp16_b1_h16_s8192_d128", "f16", 1, 16, 16, 8192, 8192, 128, False, seed=1238),
         Workload("bf16_b8_h16_kv2_sq512_sk4096_d64", "bf16", 8, 16, 2, 512, 4096, 64, False,
                  seed=1239),
+        Workload("bf16_b1_h32_kv8_s16384_d128_causal_w4096", "bf16", 1, 32, 8, 16384, 16384, 128, True,
+                 seed=1240, window=4096),
     )
 }
 

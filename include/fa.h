@@ -12,7 +12,12 @@
  *                        dQ_i  = scale * sum_j dS_ij K_j
  * dK and dV of a key/value head are summed over the H / H_kv query heads
  * that share it; query head h uses key/value head h / (H / H_kv).
- * Causal masking keeps key j for query i iff j <= i + (S_k - S_q).
+ * Query i sits at key position p_i = i + (S_k - S_q) (bottom-right alignment).
+ * Causal masking keeps key j for query i iff j <= p_i.  A sliding window of
+ * size w > 0 (fa_bwd_ex / fa_fwd_ex; boostr autograd_attention.rs carries
+ * window_size through FlashAttentionConfig into both passes, 0 = none) also
+ * drops keys with p_i - j >= w and, when not causal, keys with j - p_i >= w:
+ * a causal query sees its w most recent keys, itself included.
  *
  * Layouts (shape checks of flash_attention_bwd_impl in flash_bwd.rs and of
  * flash_attention_backward in rustytorch rtx-flash-metal-attention
@@ -96,10 +101,33 @@ int fa_bwd_preprocess(const void* dO, const void* O, float* D, int B, int H, int
  * LSE_i = log sum_j exp(scale <Q_i, K_j>) over the visible keys.
  *   Q : [B, H, S_q, d], K, V : [B, H_kv, S_k, d], O : [B, H, S_q, d] dtype;
  *   LSE : [B, H, S_q] float32.  Rows that see no key get O = 0, LSE = -inf.
- * A correctness helper computed with CUDA-core fp32 arithmetic.
+ * F16/BF16 with d in {64, 128} run a tcgen05 tensor-core kernel (fp32
+ * accumulation, online softmax over 128-key tiles); F32 runs an FFMA kernel.
  */
 int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
            int H_kv, int S_q, int S_k, int d, float scale, int causal, int dtype, void* stream);
+
+/*
+ * fa_bwd_ex / fa_fwd_ex -- fa_bwd / fa_fwd with the remaining arguments of the
+ * pages' flash_attention_bwd / flash_attention_fwd calls (boostr
+ * autograd_attention.rs, FlashAttentionBackward::backward and
+ * var_flash_attention):
+ *   window_size   : >= 0; 0 = no window, else the band described at the top.
+ *                   Key tiles outside the band are skipped, not just masked.
+ *                   A negative value gives FA_ERR_INVALID_ARG.
+ *   deterministic : 0 = dQ reduced with fp32 atomics (as fa_bwd);
+ *                   any other value gives FA_ERR_UNSUPPORTED for now.
+ * Every other argument, layout and result is that of fa_bwd / fa_fwd, which
+ * are these calls with window_size = 0 and deterministic = 0.  The pages'
+ * backward rejects window_size != 0; this library implements it.
+ */
+int fa_bwd_ex(const void* dO, const void* Q, const void* K, const void* V, const void* O,
+              const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv, int S_q,
+              int S_k, int d, float scale, int causal, int window_size, int deterministic, int dtype,
+              void* stream);
+int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+              int H_kv, int S_q, int S_k, int d, float scale, int causal, int window_size, int dtype,
+              void* stream);
 
 /*
  * fa_bwd_host -- fa_bwd on HOST buffers (same arguments and layouts, every

@@ -121,3 +121,17 @@ def test_selftest_rejects_bad_limit(lib):
     assert lib.fa_selftest_timeout(0, None) == 1
     assert fa.fa_last_error().startswith("limit_ns:")
     assert lib.fa_selftest_timeout(2_000_000_000, None) == 1
+
+
+def test_ex_entry_points_validate(lib):
+    a = [P[0], P[1], P[2], P[3], P[4], P[5], P[6], P[7], P[8], 1, 4, 2, 128, 128, 64, 0.125, 1]
+    assert lib.fa_bwd_ex(*a, -1, 0, fa.FA_BF16, None) == 1
+    assert fa.fa_last_error().startswith("window_size:")
+    assert lib.fa_bwd_ex(*a, 0, 1, fa.FA_BF16, None) == 2
+    assert fa.fa_last_error().startswith("deterministic:")
+    assert lib.fa_bwd_ex(*a[:9], 1, 5, 2, 128, 128, 64, 0.125, 1, 64, 0, fa.FA_BF16, None) == 1
+    assert fa.fa_last_error().startswith("H_kv:")
+    f = [P[0], P[1], P[2], P[3], P[4], 1, 4, 4, 8, 8, 64, 0.1, 0]
+    assert lib.fa_fwd_ex(*f, -5, fa.FA_BF16, None) == 1
+    assert fa.fa_last_error().startswith("window_size:")
+    assert lib.fa_fwd_ex(*f[:10], 96, 0.1, 0, 3, fa.FA_BF16, None) == 2

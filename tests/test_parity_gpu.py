@@ -40,16 +40,16 @@ def prepare(w: Workload):
     dev = torch.device("cuda", 0)
     g = [x.to(dev) for x in (Q, K, V, dO)]
     if w.dtype == "f32":
-        O64, L64 = oracle.ref_fwd(f64(Q), f64(K), f64(V), w.scale, w.causal)
+        O64, L64 = oracle.ref_fwd(f64(Q), f64(K), f64(V), w.scale, w.causal, w.window)
         O = torch.from_numpy(O64).to(torch.float32).to(dev)
         LSE = torch.from_numpy(L64).to(torch.float32).to(dev)
     else:
-        O, LSE = fa.fa_fwd(g[0], g[1], g[2], scale=w.scale, causal=w.causal)
+        O, LSE = fa.fa_fwd(g[0], g[1], g[2], scale=w.scale, causal=w.causal, window_size=w.window)
     return g[0], g[1], g[2], g[3], O, LSE
 
 
 def run_bwd(w, Q, K, V, dO, O, LSE):
-    dQ, dK, dV = fa.fa_bwd(dO, Q, K, V, O, LSE, scale=w.scale, causal=w.causal)
+    dQ, dK, dV = fa.fa_bwd(dO, Q, K, V, O, LSE, scale=w.scale, causal=w.causal, window_size=w.window)
     torch.cuda.synchronize()
     fa.fa_check_device()
     return dQ, dK, dV
@@ -58,7 +58,7 @@ def run_bwd(w, Q, K, V, dO, O, LSE):
 def check_full(w: Workload):
     Q, K, V, dO, O, LSE = prepare(w)
     dQ, dK, dV = run_bwd(w, Q, K, V, dO, O, LSE)
-    ref = oracle.ref_bwd(f64(dO), f64(Q), f64(K), f64(V), f64(O), f64(LSE), w.scale, w.causal)
+    ref = oracle.ref_bwd(f64(dO), f64(Q), f64(K), f64(V), f64(O), f64(LSE), w.scale, w.causal, w.window)
     tol = TOL[w.dtype]
     errs = {}
     for name, got, r in zip(("dQ", "dK", "dV"), (dQ, dK, dV), ref[:3]):
@@ -87,8 +87,8 @@ def check_sampled(w: Workload, count=256):
     rng = np.random.default_rng(7)
     qrows = sample_rows(w.B * w.H, w.S_q, count, rng)
     krows = sample_rows(w.B * w.H_kv, w.S_k, count, rng)
-    ref_dq = oracle.ref_dq_rows(*args, qrows, w.scale, w.causal)
-    ref_dk, ref_dv = oracle.ref_dkv_rows(*args, krows, w.scale, w.causal)
+    ref_dq = oracle.ref_dq_rows(*args, qrows, w.scale, w.causal, w.window)
+    ref_dk, ref_dv = oracle.ref_dkv_rows(*args, krows, w.scale, w.causal, w.window)
     got_dq = f64(dQ).reshape(-1, w.d)[qrows]
     got_dk = f64(dK).reshape(-1, w.d)[krows]
     got_dv = f64(dV).reshape(-1, w.d)[krows]
@@ -105,7 +105,8 @@ def test_workload_full(name):
 
 
 @pytest.mark.parametrize("name", ["bf16_b4_h32_kv8_s2048_d128_causal", "fp16_b1_h16_s8192_d128",
-                                  "bf16_b8_h16_kv2_sq512_sk4096_d64"])
+                                  "bf16_b8_h16_kv2_sq512_sk4096_d64",
+                                  "bf16_b1_h32_kv8_s16384_d128_causal_w4096"])
 def test_workload_sampled(name):
     check_sampled(WORKLOADS[name])
 
@@ -233,3 +234,51 @@ def test_bounded_wait_timeout_is_reported_and_context_survives():
     assert ei.value.status == 4
     fa.fa_check_device()  # the record was cleared
     check_full(Workload("after_timeout", "bf16", 1, 2, 1, 130, 130, 64, True, seed=10))
+
+
+WINDOW = [
+    # dtype, B, H, H_kv, S_q, S_k, d, causal, window
+    ("bf16", 1, 4, 2, 700, 700, 128, True, 256),    # band over several tiles, skipped on both sides
+    ("bf16", 1, 2, 1, 515, 515, 64, True, 100),     # band narrower than a tile
+    ("f16", 1, 2, 2, 400, 400, 128, False, 150),    # non-causal: band on both sides of the diagonal
+    ("bf16", 1, 2, 1, 300, 600, 128, True, 200),    # S_q < S_k
+    ("bf16", 1, 2, 1, 600, 300, 64, False, 130),    # S_q > S_k: the first rows see no key
+    ("f16", 1, 2, 1, 333, 333, 64, True, 1),        # diagonal only
+    ("bf16", 1, 2, 2, 256, 256, 128, True, 128),    # band edge on tile boundaries
+    ("bf16", 2, 4, 1, 1024, 1024, 64, True, 4096),  # wider than the problem: plain causal
+    ("f32", 1, 2, 1, 200, 200, 64, True, 37),
+    ("f32", 1, 2, 2, 150, 90, 128, False, 20),
+]
+
+
+@pytest.mark.parametrize("case", WINDOW, ids=lambda c: "-".join(map(str, c)))
+def test_sliding_window_backward(case):
+    dt, B, H, H_kv, S_q, S_k, d, causal, win = case
+    check_full(Workload("window", dt, B, H, H_kv, S_q, S_k, d, causal, seed=31, window=win))
+
+
+@pytest.mark.parametrize("case", WINDOW, ids=lambda c: "-".join(map(str, c)))
+def test_sliding_window_forward(case):
+    dt, B, H, H_kv, S_q, S_k, d, causal, win = case
+    w = Workload("window_fwd", dt, B, H, H_kv, S_q, S_k, d, causal, seed=32, window=win)
+    Q, K, V, _ = make_inputs(w)
+    O, LSE = fa.fa_fwd(Q.cuda(), K.cuda(), V.cuda(), scale=w.scale, causal=causal, window_size=win)
+    torch.cuda.synchronize()
+    fa.fa_check_device()
+    O64, L64 = oracle.ref_fwd(f64(Q), f64(K), f64(V), w.scale, causal, win)
+    assert bool(torch.isfinite(O).all())
+    assert rel_err(f64(O), O64) <= TOL[dt]
+    lse, fin = f64(LSE), np.isfinite(L64)
+    assert bool(np.all(np.isneginf(lse[~fin]))) and bool(np.all(np.isfinite(lse[fin])))
+    assert float(np.max(np.abs(lse[fin] - L64[fin]))) <= 1e-4
+
+
+def test_window_wider_than_problem_equals_no_window():
+    # the band then holds every causal pair: dK / dV bit-identical to the plain call
+    w = Workload("wide", "bf16", 1, 4, 2, 640, 640, 128, True, seed=33)
+    Q, K, V, dO, O, LSE = prepare(w)
+    a = fa.fa_bwd(dO, Q, K, V, O, LSE, scale=w.scale, causal=True)
+    b = fa.fa_bwd(dO, Q, K, V, O, LSE, scale=w.scale, causal=True, window_size=640)
+    torch.cuda.synchronize()
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    assert rel_err(f64(a[0]), f64(b[0])) < 1e-2
