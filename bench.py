@@ -298,6 +298,8 @@ def main():
                     help="time the forward (fa_fwd) on the same workload instead of the backward")
     ap.add_argument("--workload", default=BENCH_WORKLOAD, choices=sorted(WORKLOADS),
                     help="workload to time (default: the headline one)")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="time the backward with bitwise-reproducible dQ (fa_bwd_ex deterministic = 1)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -321,9 +323,10 @@ def main():
     if args.forward:
         return run_forward(args, fa, w, Q, K, V, O, LSE, flush, stream, world, rank, device)
 
+    det = bool(args.deterministic)
     for _ in range(args.warmup):
         fa.fa_bwd(dO, Q, K, V, O, LSE, scale=w.scale, causal=w.causal, dQ=dQ, dK=dK, dV=dV,
-                  window_size=w.window)
+                  window_size=w.window, deterministic=det)
     torch.cuda.synchronize(device)
     fa.fa_check_device()
 
@@ -340,7 +343,7 @@ def main():
         flush.zero_()
         starts[i].record(stream)
         fa.fa_bwd(dO, Q, K, V, O, LSE, scale=w.scale, causal=w.causal, dQ=dQ, dK=dK, dV=dV,
-                  window_size=w.window)
+                  window_size=w.window, deterministic=det)
         ends[i].record(stream)
     torch.cuda.synchronize(device)
     barrier(world)
@@ -368,9 +371,10 @@ def main():
                 "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", 1700.0)),
                 "step_frac": (flops / (ms / 1e3) / 1e12) / peak}
 
-    # ---- end to end through the host-buffer entry point (no sliding window there)
+    # ---- end to end through the host-buffer entry point (no sliding window or
+    # deterministic mode there)
     e2e = None
-    if w.window == 0:
+    if w.window == 0 and not det:
         e2e = run_e2e(args, fa, w, dO, Q, K, V, O, LSE, flops, world, device)
 
     cpu = None
@@ -384,9 +388,11 @@ def main():
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
                 "data": "synthetic (seeded normal inputs of the workload's shapes)",
                 "config": workload_config(w, {"l2": "flushed between steps (256 MiB write, outside the events)",
-                                              "parallelism": "replicas" if world > 1 else "single GPU"}),
+                                              "parallelism": "replicas" if world > 1 else "single GPU",
+                                              "deterministic_dq": det}),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": 3 * args.steps, "clocks": clocks,
+                "memset_nodes_per_step": 1 if det else 0,
                 "pct_of_bf16_peak": 100.0 * (flops / (ms / 1e3) / 1e12) / peak,
                 "timed_region_s": t_wall1 - t_wall0}
         print(json.dumps(line), flush=True)

@@ -45,7 +45,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int pad_rows(int S_q) { return (S_q + kTileQ - 1) / kTileQ * kTileQ; }
 
 struct WsLayout {
-    size_t off_err, off_lse2, off_D, off_dq, total;
+    size_t off_err, off_lse2, off_D, off_dq, off_sem, sem_bytes, total;
 };
 
 WsLayout ws_layout(int B, int H, int S_q, int d) {
@@ -55,7 +55,9 @@ WsLayout ws_layout(int B, int H, int S_q, int d) {
     L.off_lse2 = 256;
     L.off_D = align_up(L.off_lse2 + rows_pad * 4, 256);
     L.off_dq = align_up(L.off_D + rows_pad * 4, 256);
-    L.total = align_up(L.off_dq + (size_t)B * H * S_q * d * 4, 256);
+    L.off_sem = align_up(L.off_dq + (size_t)B * H * S_q * d * 4, 256);
+    L.sem_bytes = (size_t)B * H * ((S_q + kTileQ - 1) / kTileQ) * 4;
+    L.total = align_up(L.off_sem + L.sem_bytes, 256);
     return L;
 }
 
@@ -204,12 +206,15 @@ int check_window(int window) {
 
 int bwd_impl(const void* dO, const void* Q, const void* K, const void* V, const void* O,
              const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv, int S_q,
-             int S_k, int d, float scale, int causal, int window, int dtype, cudaStream_t st) {
+             int S_k, int d, float scale, int causal, int window, int deterministic, int dtype,
+             cudaStream_t st) {
     int rc;
     if ((rc = check_dims(B, H, H_kv, S_q, S_k, d, dtype))) return rc;
     if ((rc = check_scale(scale))) return rc;
     if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal", "must be 0 or 1");
     if ((rc = check_window(window))) return rc;
+    if (deterministic != 0 && deterministic != 1)
+        return fail(FA_ERR_INVALID_ARG, "deterministic", "must be 0 or 1");
     if ((rc = check_ptr(dO, "dO", 16)) || (rc = check_ptr(Q, "Q", 16)) || (rc = check_ptr(K, "K", 16)) ||
         (rc = check_ptr(V, "V", 16)) || (rc = check_ptr(O, "O", 16)) || (rc = check_ptr(LSE, "LSE", 4)) ||
         (rc = check_ptr(dQ, "dQ", 16)) || (rc = check_ptr(dK, "dK", 16)) || (rc = check_ptr(dV, "dV", 16)))
@@ -223,12 +228,18 @@ int bwd_impl(const void* dO, const void* Q, const void* K, const void* V, const 
     ws.lse2 = reinterpret_cast<float*>(static_cast<char*>(base) + L.off_lse2);
     ws.Dws = reinterpret_cast<float*>(static_cast<char*>(base) + L.off_D);
     ws.dqacc = reinterpret_cast<float*>(static_cast<char*>(base) + L.off_dq);
+    ws.dq_sem = nullptr;
     const bool tc = dtype != FA_F32 && !use_simt_for_16bit();
+    if (deterministic && tc) {
+        ws.dq_sem = reinterpret_cast<unsigned int*>(static_cast<char*>(base) + L.off_sem);
+        cudaError_t me = cudaMemsetAsync(ws.dq_sem, 0, L.sem_bytes, st);
+        if (me != cudaSuccess) return cuda_fail("turn counter reset", me);
+    }
     if (debug_enabled())
         fprintf(stderr,
-                "[fa] bwd B=%d H=%d H_kv=%d S_q=%d S_k=%d d=%d causal=%d window=%d dtype=%d kernel=%s grid=%d "
-                "ws=%zu\n",
-                B, H, H_kv, S_q, S_k, d, causal, window, dtype, tc ? "sm103" : "simt",
+                "[fa] bwd B=%d H=%d H_kv=%d S_q=%d S_k=%d d=%d causal=%d window=%d det=%d dtype=%d kernel=%s "
+                "grid=%d ws=%zu\n",
+                B, H, H_kv, S_q, S_k, d, causal, window, deterministic, dtype, tc ? "sm103" : "simt",
                 tc ? (S_k + kTileK - 1) / kTileK * B * H_kv : 0, L.total);
     ProfRec pr;
     const bool prof = prof_begin(&pr);
@@ -236,8 +247,14 @@ int bwd_impl(const void* dO, const void* Q, const void* K, const void* V, const 
     cudaError_t e = launch_preprocess(dtype, dO, O, LSE, ws.Dws, ws.lse2, ws.dqacc, s, s.S_q_pad, st);
     if (e != cudaSuccess) return cuda_fail("preprocess launch", e);
     if (prof) cudaEventRecord(pr.ev[1], st);
-    e = tc ? launch_bwd_sm103(dtype, Q, K, V, dO, ws, dK, dV, s, st)
-           : launch_bwd_simt(dtype, Q, K, V, dO, ws, dK, dV, s, st);
+    if (tc) {
+        e = launch_bwd_sm103(dtype, Q, K, V, dO, ws, dK, dV, s, st);
+    } else {
+        // CUDA-core path: deterministic dQ comes from its own kernel, which sums each row's
+        // contributions in key order; the main kernel then leaves dQ alone
+        e = launch_bwd_simt(dtype, Q, K, V, dO, ws, dK, dV, s, deterministic != 0, st);
+        if (e == cudaSuccess && deterministic) e = launch_dq_simt(dtype, Q, K, V, dO, ws, s, st);
+    }
     if (e != cudaSuccess) return cuda_fail("main kernel launch", e);
     if (prof) cudaEventRecord(pr.ev[2], st);
     e = launch_dq_finalize(dtype, ws.dqacc, dQ, s, st);
@@ -320,7 +337,7 @@ int fa_bwd(const void* dO, const void* Q, const void* K, const void* V, const vo
            const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv, int S_q,
            int S_k, int d, float scale, int causal, int dtype, void* stream) {
     g_last_error.clear();
-    return bwd_impl(dO, Q, K, V, O, LSE, dQ, dK, dV, B, H, H_kv, S_q, S_k, d, scale, causal, 0, dtype,
+    return bwd_impl(dO, Q, K, V, O, LSE, dQ, dK, dV, B, H, H_kv, S_q, S_k, d, scale, causal, 0, 0, dtype,
                     static_cast<cudaStream_t>(stream));
 }
 
@@ -329,10 +346,8 @@ int fa_bwd_ex(const void* dO, const void* Q, const void* K, const void* V, const
               int S_k, int d, float scale, int causal, int window_size, int deterministic, int dtype,
               void* stream) {
     g_last_error.clear();
-    if (deterministic != 0)
-        return fail(FA_ERR_UNSUPPORTED, "deterministic", "only 0 (fp32 atomic dQ reduction) is available");
     return bwd_impl(dO, Q, K, V, O, LSE, dQ, dK, dV, B, H, H_kv, S_q, S_k, d, scale, causal, window_size,
-                    dtype, static_cast<cudaStream_t>(stream));
+                    deterministic, dtype, static_cast<cudaStream_t>(stream));
 }
 
 int fa_bwd_preprocess(const void* dO, const void* O, float* D, int B, int H, int S_q, int d,
@@ -454,7 +469,7 @@ int fa_bwd_host(const void* dO, const void* Q, const void* K, const void* V, con
             return cuda_fail("cudaEventRecord / cudaStreamWaitEvent", e);
         auto at = [&](int slot) { return dbase + off[slot] + u0 * unit_bytes(slot); };
         rc = bwd_impl(at(0), at(1), at(4), at(5), at(2), reinterpret_cast<const float*>(at(8)), at(3), at(6), at(7),
-                      1, nu * g, nu, S_q, S_k, d, scale, causal, 0, dtype, st);
+                      1, nu * g, nu, S_q, S_k, d, scale, causal, 0, 0, dtype, st);
         if (rc != FA_OK) return rc;
         if ((e = cudaEventRecord(hs->ev_done[c], st)) != cudaSuccess ||
             (e = cudaStreamWaitEvent(hs->s_out, hs->ev_done[c], 0)) != cudaSuccess)

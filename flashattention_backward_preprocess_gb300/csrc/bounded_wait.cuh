@@ -40,6 +40,26 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, vol
     return __all_sync(0xffffffffu, ok);
 }
 
+// Bounded wait until a counter in global memory, advanced by other CTAs of the same launch
+// (release stores), reaches `want`; acquire ordering on success.  Polls every ~100 ns.
+// The CTAs waited for have lower block indices, so they were dispatched earlier.
+__device__ __forceinline__ bool wait_counter(const unsigned int* ctr, unsigned int want,
+                                             volatile int* abort_flag, unsigned int* err,
+                                             uint64_t limit_ns = kWaitLimitNs) {
+    if (ptx::ld_acquire_gpu(ctr) >= want) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    while (true) {
+        __nanosleep(100);
+        if (ptx::ld_acquire_gpu(ctr) >= want) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer() - t0 > limit_ns) {
+            *abort_flag = 1;
+            atomicOr(err, kErrTimeout);
+            return false;
+        }
+    }
+}
+
 // Wait used while shutting down after an abort: bounded, no flag checks.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     const uint64_t t0 = ptx::globaltimer();

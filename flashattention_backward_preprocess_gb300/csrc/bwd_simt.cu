@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_kernel(
                     sdK[j * D + c] = fmaf(sds[j], qc, sdK[j * D + c]);
                     acc = fmaf(sds[j], sK[j * D + c], acc);
                 }
-                atomicAdd(dqacc + qi + c, acc);
+                if (dqacc != nullptr) atomicAdd(dqacc + qi + c, acc);  // null: dQ by dq_simt_kernel
             }
             __syncthreads();
         }
@@ -117,9 +117,93 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_kernel(
     }
 }
 
+// Deterministic dQ on CUDA cores: one CTA per (kDqRows-row query block, query head) forms
+//   dQacc_i = sum_j dS_ij K_j,  dS_ij = P_ij (<dO_i, V_j> - D_i),  P_ij = exp(scale <Q_i, K_j> - LSE_i)
+// itself, visiting the visible keys in increasing index order, so every row is one fixed
+// sequence of fp32 additions (no atomics).  S and dP are recomputed from Q, K, V, dO.
+constexpr int kDqRows = 16;  // query rows per CTA
+constexpr int kDqKeys = 32;  // keys per step
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) dq_simt_kernel(
+    const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
+    const T* __restrict__ dO, const float* __restrict__ lse2, const float* __restrict__ Dws,
+    float* __restrict__ dqacc, Shape s) {
+    extern __shared__ float smem[];
+    float* sQ = smem;                     // [kDqRows][D]
+    float* sdO = sQ + kDqRows * D;        // [kDqRows][D]
+    float* sK = sdO + kDqRows * D;        // [kDqKeys][D]
+    float* sV = sK + kDqKeys * D;         // [kDqKeys][D]
+    float* sdS = sV + kDqKeys * D;        // [kDqRows][kDqKeys]
+    constexpr int kRowsPerThread = kDqRows * D / kThreads;
+    static_assert(kRowsPerThread * kThreads == kDqRows * D, "thread split of the dQ block");
+    constexpr int kRowStep = kThreads / D;  // a thread owns column c, rows r0, r0 + kRowStep, ...
+
+    const int tid = threadIdx.x;
+    const int m0 = blockIdx.x * kDqRows;
+    const int bh = blockIdx.y;
+    const int b = bh / s.H, h = bh % s.H;
+    const int bkv = b * s.H_kv + h / (s.H / s.H_kv);
+    const int off = s.S_k - s.S_q;
+    const float kLog2e = 1.4426950408889634f;
+    const int rows = min(kDqRows, s.S_q - m0);
+
+    for (int e = tid; e < kDqRows * D; e += kThreads) {
+        const int r = e / D, c = e % D;
+        const size_t gi = ((size_t)bh * s.S_q + m0 + r) * D + c;
+        sQ[e] = r < rows ? TypeTraits<T>::to_f32(Q[gi]) : 0.f;
+        sdO[e] = r < rows ? TypeTraits<T>::to_f32(dO[gi]) : 0.f;
+    }
+    const int c_own = tid % D, r_own = tid / D;
+    float acc[kRowsPerThread];
+#pragma unroll
+    for (int a = 0; a < kRowsPerThread; ++a) acc[a] = 0.f;
+
+    int k_lo, k_hi;
+    key_range(s, m0, m0 + rows, k_lo, k_hi);
+    for (int n0 = k_lo - k_lo % kDqKeys; n0 < k_hi; n0 += kDqKeys) {
+        __syncthreads();  // previous step's sK / sdS reads are done
+        for (int e = tid; e < kDqKeys * D; e += kThreads) {
+            const int j = n0 + e / D;
+            const size_t gi = ((size_t)bkv * s.S_k + j) * D + e % D;
+            sK[e] = j < s.S_k ? TypeTraits<T>::to_f32(K[gi]) : 0.f;
+            sV[e] = j < s.S_k ? TypeTraits<T>::to_f32(V[gi]) : 0.f;
+        }
+        __syncthreads();
+        for (int pr = tid; pr < kDqRows * kDqKeys; pr += kThreads) {
+            const int r = pr / kDqKeys, jj = pr % kDqKeys;
+            const int i = m0 + r, j = n0 + jj;
+            float ds = 0.f;
+            if (r < rows && j < s.S_k && key_visible(i + off, j, s.causal, s.window)) {
+                float sc = 0.f, dp = 0.f;
+                for (int c = 0; c < D; ++c) {
+                    sc = fmaf(sQ[r * D + c], sK[jj * D + c], sc);
+                    dp = fmaf(sdO[r * D + c], sV[jj * D + c], dp);
+                }
+                const size_t row = (size_t)bh * s.S_q_pad + i;
+                const float p = exp2f(fmaf(sc, s.scale * kLog2e, -lse2[row]));
+                ds = p * (dp - Dws[row]);
+            }
+            sdS[pr] = ds;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int a = 0; a < kRowsPerThread; ++a) {
+            const int r = r_own + a * kRowStep;
+            for (int jj = 0; jj < kDqKeys; ++jj) acc[a] = fmaf(sdS[r * kDqKeys + jj], sK[jj * D + c_own], acc[a]);
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < kRowsPerThread; ++a) {
+        const int r = r_own + a * kRowStep;
+        if (r < rows) dqacc[((size_t)bh * s.S_q + m0 + r) * D + c_own] = acc[a];
+    }
+}
+
 template <typename T, int D>
 cudaError_t launch_t(const void* Q, const void* K, const void* V, const void* dO,
-                     const Workspace& ws, void* dK, void* dV, const Shape& s, cudaStream_t st) {
+                     const Workspace& ws, void* dK, void* dV, const Shape& s, bool skip_dq,
+                     cudaStream_t st) {
     const size_t smem = sizeof(float) * (4 * kTile * D + 2 * D + 2 * kTile);
     auto kern = bwd_simt_kernel<T, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -127,17 +211,47 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, const void* dO
     dim3 grid((s.S_k + kTile - 1) / kTile, s.B * s.H_kv);
     kern<<<grid, kThreads, smem, st>>>(static_cast<const T*>(Q), static_cast<const T*>(K),
                                        static_cast<const T*>(V), static_cast<const T*>(dO),
-                                       ws.lse2, ws.Dws, ws.dqacc, static_cast<T*>(dK),
+                                       ws.lse2, ws.Dws, skip_dq ? nullptr : ws.dqacc, static_cast<T*>(dK),
                                        static_cast<T*>(dV), s);
+    return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_dq_t(const void* Q, const void* K, const void* V, const void* dO, const Workspace& ws,
+                        const Shape& s, cudaStream_t st) {
+    const size_t smem = sizeof(float) * (2 * kDqRows * D + 2 * kDqKeys * D + kDqRows * kDqKeys);
+    auto kern = dq_simt_kernel<T, D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((s.S_q + kDqRows - 1) / kDqRows, s.B * s.H);
+    kern<<<grid, kThreads, smem, st>>>(static_cast<const T*>(Q), static_cast<const T*>(K),
+                                       static_cast<const T*>(V), static_cast<const T*>(dO), ws.lse2, ws.Dws,
+                                       ws.dqacc, s);
     return cudaGetLastError();
 }
 
 }  // namespace
 
+cudaError_t launch_dq_simt(int dtype, const void* Q, const void* K, const void* V, const void* dO,
+                           const Workspace& ws, const Shape& s, cudaStream_t st) {
+#define FA_L(T, DD) return launch_dq_t<T, DD>(Q, K, V, dO, ws, s, st)
+    if (s.d == 64) {
+        if (dtype == FA_F32) FA_L(float, 64);
+        if (dtype == FA_F16) FA_L(__half, 64);
+        if (dtype == FA_BF16) FA_L(__nv_bfloat16, 64);
+    } else if (s.d == 128) {
+        if (dtype == FA_F32) FA_L(float, 128);
+        if (dtype == FA_F16) FA_L(__half, 128);
+        if (dtype == FA_BF16) FA_L(__nv_bfloat16, 128);
+    }
+#undef FA_L
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_bwd_simt(int dtype, const void* Q, const void* K, const void* V,
                             const void* dO, const Workspace& ws, void* dK, void* dV,
-                            const Shape& s, cudaStream_t st) {
-#define FA_L(T, DD) return launch_t<T, DD>(Q, K, V, dO, ws, dK, dV, s, st)
+                            const Shape& s, bool skip_dq, cudaStream_t st) {
+#define FA_L(T, DD) return launch_t<T, DD>(Q, K, V, dO, ws, dK, dV, s, skip_dq, st)
     if (s.d == 64) {
         if (dtype == FA_F32) FA_L(float, 64);
         if (dtype == FA_F16) FA_L(__half, 64);

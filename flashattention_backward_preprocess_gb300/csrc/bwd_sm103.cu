@@ -108,6 +108,7 @@ struct Params {
     void* dK;
     void* dV;
     unsigned int* err;
+    unsigned int* dq_sem;  // deterministic dQ: [B*H][query tiles] turn counters, else nullptr
     int B, H, H_kv, S_q, S_k, S_q_pad;
     float scale, scale_log2;
     int causal, window;
@@ -168,15 +169,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int off = p.S_k - p.S_q;  // query i sits at key position i + off
     // query tiles [m_start, m_end) hold every row that sees a key of this tile (causal
     // edge below, sliding-window band edges on either side)
+    Shape sh;  // the fields the range helpers read
+    sh.S_q = p.S_q;
+    sh.S_k = p.S_k;
+    sh.causal = p.causal;
+    sh.window = p.window;
     int q_lo, q_hi;
-    {
-        Shape sh;
-        sh.S_q = p.S_q;
-        sh.S_k = p.S_k;
-        sh.causal = p.causal;
-        sh.window = p.window;
-        query_range(sh, n0, min(n0 + BN, p.S_k), q_lo, q_hi);
-    }
+    query_range(sh, n0, min(n0 + BN, p.S_k), q_lo, q_hi);
+    const int m_tiles = (p.S_q + BM - 1) / BM;
     const int m_start = q_lo / BM;
     const int m_end = q_hi > q_lo ? (q_hi + BM - 1) / BM : m_start;
     const int nm = m_end - m_start;
@@ -496,6 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const bool issuer = t == 0;
         bool ok = !*abort_flag;
+        unsigned int* prev_sem = nullptr;  // deterministic dQ: turn to pass on once complete
+        unsigned int prev_turn = 0;
         for (int it = 0; ok && it < n_it; ++it) {
             const int s = it % C::STAGES;
             const uint32_t X = tm_buf0 + 128 * (it & 1) + lane_off;
@@ -534,11 +536,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::fence_proxy_async_smem();
             ptx::named_bar_sync(kDrainBarrier, 128);
             if (issuer) {
+                // Deterministic dQ: the key tiles that touch this query tile add into it in
+                // key-tile order.  Turn t of the tile's counter belongs to its t-th such key
+                // tile (they are consecutive: the first is where key_range of the query tile
+                // starts).  Wait for the turn, add, and pass it on once the adds are complete:
+                // one iteration later, so the drain never waits for its own reduce.  Holding
+                // that turn meanwhile cannot deadlock: only CTAs of higher block index wait
+                // for it, and this CTA never waits for one of those.
+                unsigned int* sem = nullptr;
+                unsigned int turn = 0;
+                bool go = true;
+                if (p.dq_sem != nullptr) {
+                    int k_lo, k_hi;
+                    key_range(sh, m0, min(m0 + BM, p.S_q), k_lo, k_hi);
+                    turn = (unsigned int)(n_tile - k_lo / BN);
+                    sem = p.dq_sem + (size_t)bh * m_tiles + m0 / BM;
+                    go = wait_counter(sem, turn, abort_flag, p.err);
+                    ptx::fence_proxy_async_global();  // the earlier turns' adds before ours
+                }
 #pragma unroll
                 for (int h = 0; h < D / 64; ++h) {  // one bulk group per staging area, dS tile first
                     const uint32_t area = sbase + (h == 0 ? C::OFF_DS : C::OFF_DO + s * C::kTileQ_B);
-                    ptx::tma_reduce_add_3d(&tmdQ, area, h * 64, m0, bh);
-                    ptx::tma_reduce_add_3d(&tmdQ, area + BM * 128, h * 64 + 32, m0, bh);
+                    if (go) {
+                        ptx::tma_reduce_add_3d(&tmdQ, area, h * 64, m0, bh);
+                        ptx::tma_reduce_add_3d(&tmdQ, area + BM * 128, h * 64 + 32, m0, bh);
+                    }
                     ptx::bulk_commit_group();
                 }
                 if (D == 128) {
@@ -550,9 +572,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::bulk_wait_read_all();
                     ptx::mbar_arrive(bar(B_DS_EMPTY));
                 }
+                if (prev_sem != nullptr) {
+                    // the previous tile's groups are complete once at most this tile's are pending
+                    ptx::bulk_wait_pending<D / 64>();
+                    ptx::fence_proxy_async_global();  // its adds before the next turn's
+                    ptx::st_release_gpu(prev_sem, prev_turn + 1);
+                }
+                prev_sem = go ? sem : nullptr;
+                prev_turn = turn;
             }
         }
-        if (issuer) ptx::bulk_wait_all();
+        if (issuer) {
+            ptx::bulk_wait_all();
+            if (prev_sem != nullptr) {
+                ptx::fence_proxy_async_global();
+                ptx::st_release_gpu(prev_sem, prev_turn + 1);
+            }
+        }
     }
 
     ptx::tc_fence_before();
@@ -615,6 +651,7 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, const void* dO
     p.dK = dK;
     p.dV = dV;
     p.err = ws.err;
+    p.dq_sem = ws.dq_sem;
     p.B = s.B;
     p.H = s.H;
     p.H_kv = s.H_kv;

@@ -105,6 +105,9 @@ struct Workspace {
     float* lse2;        // [B*H][S_q_pad] LSE * log2(e), +inf on padding / empty rows
     float* Dws;         // [B*H][S_q_pad] D = rowsum(dO * O), 0 on padding
     float* dqacc;       // [B*H][S_q][d] fp32 dQ accumulator (unscaled)
+    // [B*H][ceil(S_q / 128)] turn counters of the deterministic dQ reduction (zeroed per
+    // call), or nullptr: then dQ tiles are reduced in whatever order the CTAs reach them
+    unsigned int* dq_sem;
 };
 
 constexpr int kTileQ = 128;  // query rows per main-kernel iteration
@@ -116,10 +119,13 @@ cudaError_t launch_preprocess(int dtype, const void* dO, const void* O, const fl
                               int rows_stride, cudaStream_t st);
 cudaError_t launch_dq_finalize(int dtype, const float* dqacc, void* dQ, const Shape& s,
                                cudaStream_t st);
-// bwd_simt.cu (fp32 path)
+// bwd_simt.cu (fp32 path).  skip_dq: leave the dQ accumulator alone (launch_dq_simt fills it).
 cudaError_t launch_bwd_simt(int dtype, const void* Q, const void* K, const void* V,
                             const void* dO, const Workspace& ws, void* dK, void* dV,
-                            const Shape& s, cudaStream_t st);
+                            const Shape& s, bool skip_dq, cudaStream_t st);
+// Deterministic dQ accumulator rows on CUDA cores (each row summed over keys in index order).
+cudaError_t launch_dq_simt(int dtype, const void* Q, const void* K, const void* V, const void* dO,
+                           const Workspace& ws, const Shape& s, cudaStream_t st);
 // fwd_simt.cu
 cudaError_t launch_fwd_simt(int dtype, const void* Q, const void* K, const void* V, void* O,
                             float* LSE, const Shape& s, cudaStream_t st);

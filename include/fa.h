@@ -79,7 +79,8 @@ typedef enum {
  * F16/BF16 run the tcgen05 tensor-core kernel; F32 runs an FFMA kernel.
  * dQ is reduced across key tiles with fp32 atomics, so dQ may differ in the
  * last bits between runs (flash_bwd.rs, "dQ must be zeroed -- backward uses
- * atomicAdd"); dK and dV are deterministic.
+ * atomicAdd"); dK and dV are deterministic.  fa_bwd_ex(..., deterministic = 1)
+ * makes dQ reproducible too.
  */
 int fa_bwd(const void* dO, const void* Q, const void* K, const void* V, const void* O,
            const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv, int S_q,
@@ -115,11 +116,19 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int
  *   window_size   : >= 0; 0 = no window, else the band described at the top.
  *                   Key tiles outside the band are skipped, not just masked.
  *                   A negative value gives FA_ERR_INVALID_ARG.
- *   deterministic : 0 = dQ reduced with fp32 atomics (as fa_bwd);
- *                   any other value gives FA_ERR_UNSUPPORTED for now.
- * Every other argument, layout and result is that of fa_bwd / fa_fwd, which
- * are these calls with window_size = 0 and deterministic = 0.  The pages'
- * backward rejects window_size != 0; this library implements it.
+ *   deterministic : 0 = dQ reduced with fp32 atomics (as fa_bwd; the pages'
+ *                   atomicAdd accumulation), bits may vary between runs;
+ *                   1 = bitwise reproducible dQ: F16/BF16 add each 128x128
+ *                   dQ tile's per-key-tile contributions in key-tile order
+ *                   (the CTAs pass a turn counter in the workspace along; a
+ *                   CTA only ever waits for CTAs with lower block indices of
+ *                   the same launch, and every wait is bounded); F32 computes
+ *                   dQ in its own kernel, each row summed over keys in index
+ *                   order.  Other values give FA_ERR_INVALID_ARG.
+ * dK and dV are bitwise reproducible in both modes.  Every other argument,
+ * layout and result is that of fa_bwd / fa_fwd, which are these calls with
+ * window_size = 0 and deterministic = 0.  The pages' backward rejects
+ * window_size != 0; this library implements it.
  */
 int fa_bwd_ex(const void* dO, const void* Q, const void* K, const void* V, const void* O,
               const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv, int S_q,
@@ -169,8 +178,9 @@ int fa_bwd_noalloc(const void* dO, const void* Q, const void* K, const void* V, 
                    const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv,
                    int S_q, int S_k, int d, float scale, int causal, int dtype, void* stream);
 
-/* Workspace bytes fa_bwd needs for a shape (informational; the library
- * allocates and caches it itself). */
+/* Workspace bytes fa_bwd / fa_bwd_ex need for a shape (informational; the
+ * library allocates and caches it itself): error words, padded LSE and D
+ * copies, the fp32 dQ accumulator and the deterministic mode's turn counters. */
 size_t fa_bwd_workspace_bytes(int B, int H, int S_q, int d);
 
 /* Synchronizes `stream`, then returns FA_ERR_TIMEOUT if a kernel of this

@@ -96,10 +96,11 @@ def test_preprocess_and_fwd_validate(lib):
 
 
 def test_workspace_bytes(lib):
-    # err words, padded LSE*log2e and D copies (rows padded to 128), fp32 dQ accumulator
+    # err words, padded LSE*log2e and D copies (rows padded to 128), fp32 dQ accumulator,
+    # one turn counter per (query head, 128-row query tile) for the deterministic dQ mode
     B, H, S, d = 4, 32, 2048, 128
     rows = B * H * S
-    assert fa.fa_bwd_workspace_bytes(B, H, S, d) == 256 + 2 * rows * 4 + rows * d * 4
+    assert fa.fa_bwd_workspace_bytes(B, H, S, d) == 256 + 2 * rows * 4 + rows * d * 4 + B * H * (S // 128) * 4
     B, H, S, d = 1, 2, 200, 64
     rows_pad = B * H * 256
     got = fa.fa_bwd_workspace_bytes(B, H, S, d)
@@ -127,7 +128,7 @@ def test_ex_entry_points_validate(lib):
     a = [P[0], P[1], P[2], P[3], P[4], P[5], P[6], P[7], P[8], 1, 4, 2, 128, 128, 64, 0.125, 1]
     assert lib.fa_bwd_ex(*a, -1, 0, fa.FA_BF16, None) == 1
     assert fa.fa_last_error().startswith("window_size:")
-    assert lib.fa_bwd_ex(*a, 0, 1, fa.FA_BF16, None) == 2
+    assert lib.fa_bwd_ex(*a, 0, 2, fa.FA_BF16, None) == 1
     assert fa.fa_last_error().startswith("deterministic:")
     assert lib.fa_bwd_ex(*a[:9], 1, 5, 2, 128, 128, 64, 0.125, 1, 64, 0, fa.FA_BF16, None) == 1
     assert fa.fa_last_error().startswith("H_kv:")

@@ -282,3 +282,53 @@ def test_window_wider_than_problem_equals_no_window():
     torch.cuda.synchronize()
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
     assert rel_err(f64(a[0]), f64(b[0])) < 1e-2
+
+
+DET = [
+    # dtype, B, H, H_kv, S_q, S_k, d, causal, window
+    ("bf16", 2, 8, 2, 700, 700, 128, True, 0),      # causal, GQA 4, ragged tail
+    ("f16", 1, 4, 4, 513, 300, 64, False, 0),       # S_q > S_k, d = 64
+    ("bf16", 1, 4, 1, 300, 600, 128, True, 200),    # window: turns start past key tile 0
+    ("bf16", 1, 2, 2, 600, 600, 64, False, 130),    # two-sided window
+    ("f32", 1, 4, 2, 200, 333, 128, True, 0),       # CUDA-core dQ kernel
+    ("f32", 1, 2, 1, 150, 150, 64, False, 40),
+]
+
+
+@pytest.mark.parametrize("case", DET, ids=lambda c: "-".join(map(str, c)))
+def test_deterministic_dq_matches_oracle_and_is_reproducible(case):
+    dt, B, H, H_kv, S_q, S_k, d, causal, win = case
+    w = Workload("det_dq", dt, B, H, H_kv, S_q, S_k, d, causal, seed=41, window=win)
+    Q, K, V, dO, O, LSE = prepare(w)
+    runs = []
+    for _ in range(3):
+        runs.append(fa.fa_bwd(dO, Q, K, V, O, LSE, scale=w.scale, causal=causal, window_size=win,
+                              deterministic=True))
+        torch.cuda.synchronize()
+        fa.fa_check_device()
+    for r in runs[1:]:
+        for a, b in zip(runs[0], r):
+            assert torch.equal(a, b)
+    ref = oracle.ref_bwd(f64(dO), f64(Q), f64(K), f64(V), f64(O), f64(LSE), w.scale, causal, win)
+    for name, got, r in zip(("dQ", "dK", "dV"), runs[0], ref[:3]):
+        assert rel_err(f64(got), r) <= TOL[dt], name
+    # dK / dV do not depend on how dQ is reduced
+    nd = fa.fa_bwd(dO, Q, K, V, O, LSE, scale=w.scale, causal=causal, window_size=win)
+    torch.cuda.synchronize()
+    assert torch.equal(nd[1], runs[0][1]) and torch.equal(nd[2], runs[0][2])
+
+
+def test_deterministic_dq_bench_workload_bitwise():
+    # full size, as the benchmark launches it: two deterministic calls give the same dQ bits,
+    # and sampled rows match the oracle
+    w = WORKLOADS["bf16_b4_h32_kv8_s2048_d128_causal"]
+    Q, K, V, dO, O, LSE = prepare(w)
+    a = fa.fa_bwd(dO, Q, K, V, O, LSE, scale=w.scale, causal=True, deterministic=True)
+    b = fa.fa_bwd(dO, Q, K, V, O, LSE, scale=w.scale, causal=True, deterministic=True)
+    torch.cuda.synchronize()
+    fa.fa_check_device()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    args = [f64(x) for x in (dO, Q, K, V, O, LSE)]
+    qrows = sample_rows(w.B * w.H, w.S_q, 128, np.random.default_rng(3))
+    ref = oracle.ref_dq_rows(*args, qrows, w.scale, True)
+    assert rel_err(f64(a[0]).reshape(-1, w.d)[qrows], ref) <= TOL[w.dtype]
