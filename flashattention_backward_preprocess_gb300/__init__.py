@@ -3,7 +3,8 @@ then dQ, dK, dV from a tcgen05 tensor-core kernel.
 
 The compute lives in the C-ABI library ``_build/libfa.so`` (include/fa.h);
 this package is the thin Python binding over it (argument marshalling only,
-via ctypes) plus the seeded input generators (``inputs``).  Functions take
+via ctypes), a torch.autograd.Function over the forward and backward
+(``autograd``) and the seeded input generators (``inputs``).  Functions take
 torch CUDA tensors; every step of the path runs in the library's kernels.
 If the library is missing or cannot be loaded the calls raise: there is no
 fallback.
@@ -29,3 +30,4 @@ from .binding import (  # noqa: F401
     library_path,
     load_library,
 )
+from .autograd import FlashAttentionFunction, flash_attention  # noqa: F401

@@ -115,8 +115,9 @@ int check_dims(int B, int H, int H_kv, int S_q, int S_k, int d, int dtype) {
     if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16)
         return fail(FA_ERR_INVALID_ARG, "dtype", "unsupported dtype " + std::to_string(dtype) +
                                                      " (expected FA_F32, FA_F16 or FA_BF16)");
-    if (d != 64 && d != 128)
-        return fail(FA_ERR_UNSUPPORTED, "d", "head dim " + std::to_string(d) + " not supported (64 or 128)");
+    if (!head_dim_supported(d))
+        return fail(FA_ERR_UNSUPPORTED, "d",
+                    "head dim " + std::to_string(d) + " not supported (32, 64, 96, 128 or 256)");
     // every flattened index must fit the kernels' 32-bit row arithmetic
     const double rows_q = (double)B * H * (double)pad_rows(S_q);
     const double rows_k = (double)B * H_kv * (double)S_k;
@@ -229,7 +230,8 @@ int bwd_impl(const void* dO, const void* Q, const void* K, const void* V, const 
     ws.Dws = reinterpret_cast<float*>(static_cast<char*>(base) + L.off_D);
     ws.dqacc = reinterpret_cast<float*>(static_cast<char*>(base) + L.off_dq);
     ws.dq_sem = nullptr;
-    const bool tc = dtype != FA_F32 && !use_simt_for_16bit();
+    // tensor cores for f16 / bf16 at head dims up to 128; CUDA cores for f32 and d = 256
+    const bool tc = dtype != FA_F32 && !use_simt_for_16bit() && tc_head_dim(d) != 0;
     if (deterministic && tc) {
         ws.dq_sem = reinterpret_cast<unsigned int*>(static_cast<char*>(base) + L.off_sem);
         cudaError_t me = cudaMemsetAsync(ws.dq_sem, 0, L.sem_bytes, st);
@@ -278,7 +280,7 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
         return rc;
     const Shape s = make_shape(B, H, H_kv, S_q, S_k, d, scale, causal, window);
     cudaError_t e;
-    if (dtype == FA_F32 || fwd_simt_for_16bit()) {
+    if (dtype == FA_F32 || fwd_simt_for_16bit() || tc_head_dim(d) == 0) {
         e = launch_fwd_simt(dtype, Q, K, V, O, LSE, s, st);
     } else {
         // the tensor-core forward reports bounded-wait timeouts in the stream's workspace

@@ -135,9 +135,8 @@ __global__ void __launch_bounds__(kThreads) dq_simt_kernel(
     float* sK = sdO + kDqRows * D;        // [kDqKeys][D]
     float* sV = sK + kDqKeys * D;         // [kDqKeys][D]
     float* sdS = sV + kDqKeys * D;        // [kDqRows][kDqKeys]
-    constexpr int kRowsPerThread = kDqRows * D / kThreads;
-    static_assert(kRowsPerThread * kThreads == kDqRows * D, "thread split of the dQ block");
-    constexpr int kRowStep = kThreads / D;  // a thread owns column c, rows r0, r0 + kRowStep, ...
+    constexpr int kPerThread = kDqRows * D / kThreads;  // dQ elements a thread accumulates
+    static_assert(kPerThread * kThreads == kDqRows * D, "thread split of the dQ block");
 
     const int tid = threadIdx.x;
     const int m0 = blockIdx.x * kDqRows;
@@ -154,10 +153,10 @@ __global__ void __launch_bounds__(kThreads) dq_simt_kernel(
         sQ[e] = r < rows ? TypeTraits<T>::to_f32(Q[gi]) : 0.f;
         sdO[e] = r < rows ? TypeTraits<T>::to_f32(dO[gi]) : 0.f;
     }
-    const int c_own = tid % D, r_own = tid / D;
-    float acc[kRowsPerThread];
+    // thread tid owns block elements e = tid + a * kThreads: row e / D, column e % D
+    float acc[kPerThread];
 #pragma unroll
-    for (int a = 0; a < kRowsPerThread; ++a) acc[a] = 0.f;
+    for (int a = 0; a < kPerThread; ++a) acc[a] = 0.f;
 
     int k_lo, k_hi;
     key_range(s, m0, m0 + rows, k_lo, k_hi);
@@ -188,15 +187,15 @@ __global__ void __launch_bounds__(kThreads) dq_simt_kernel(
         }
         __syncthreads();
 #pragma unroll
-        for (int a = 0; a < kRowsPerThread; ++a) {
-            const int r = r_own + a * kRowStep;
-            for (int jj = 0; jj < kDqKeys; ++jj) acc[a] = fmaf(sdS[r * kDqKeys + jj], sK[jj * D + c_own], acc[a]);
+        for (int a = 0; a < kPerThread; ++a) {
+            const int e = tid + a * kThreads, r = e / D, c = e % D;
+            for (int jj = 0; jj < kDqKeys; ++jj) acc[a] = fmaf(sdS[r * kDqKeys + jj], sK[jj * D + c], acc[a]);
         }
     }
 #pragma unroll
-    for (int a = 0; a < kRowsPerThread; ++a) {
-        const int r = r_own + a * kRowStep;
-        if (r < rows) dqacc[((size_t)bh * s.S_q + m0 + r) * D + c_own] = acc[a];
+    for (int a = 0; a < kPerThread; ++a) {
+        const int e = tid + a * kThreads, r = e / D, c = e % D;
+        if (r < rows) dqacc[((size_t)bh * s.S_q + m0 + r) * D + c] = acc[a];
     }
 }
 
@@ -235,15 +234,7 @@ cudaError_t launch_dq_t(const void* Q, const void* K, const void* V, const void*
 cudaError_t launch_dq_simt(int dtype, const void* Q, const void* K, const void* V, const void* dO,
                            const Workspace& ws, const Shape& s, cudaStream_t st) {
 #define FA_L(T, DD) return launch_dq_t<T, DD>(Q, K, V, dO, ws, s, st)
-    if (s.d == 64) {
-        if (dtype == FA_F32) FA_L(float, 64);
-        if (dtype == FA_F16) FA_L(__half, 64);
-        if (dtype == FA_BF16) FA_L(__nv_bfloat16, 64);
-    } else if (s.d == 128) {
-        if (dtype == FA_F32) FA_L(float, 128);
-        if (dtype == FA_F16) FA_L(__half, 128);
-        if (dtype == FA_BF16) FA_L(__nv_bfloat16, 128);
-    }
+    FA_DISPATCH_HEAD_DIM(dtype, s.d, FA_L);
 #undef FA_L
     return cudaErrorInvalidValue;
 }
@@ -252,15 +243,7 @@ cudaError_t launch_bwd_simt(int dtype, const void* Q, const void* K, const void*
                             const void* dO, const Workspace& ws, void* dK, void* dV,
                             const Shape& s, bool skip_dq, cudaStream_t st) {
 #define FA_L(T, DD) return launch_t<T, DD>(Q, K, V, dO, ws, dK, dV, s, skip_dq, st)
-    if (s.d == 64) {
-        if (dtype == FA_F32) FA_L(float, 64);
-        if (dtype == FA_F16) FA_L(__half, 64);
-        if (dtype == FA_BF16) FA_L(__nv_bfloat16, 64);
-    } else if (s.d == 128) {
-        if (dtype == FA_F32) FA_L(float, 128);
-        if (dtype == FA_F16) FA_L(__half, 128);
-        if (dtype == FA_BF16) FA_L(__nv_bfloat16, 128);
-    }
+    FA_DISPATCH_HEAD_DIM(dtype, s.d, FA_L);
 #undef FA_L
     return cudaErrorInvalidValue;
 }

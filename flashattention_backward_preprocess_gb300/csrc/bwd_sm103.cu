@@ -110,6 +110,7 @@ struct Params {
     unsigned int* err;
     unsigned int* dq_sem;  // deterministic dQ: [B*H][query tiles] turn counters, else nullptr
     int B, H, H_kv, S_q, S_k, S_q_pad;
+    int d;  // head dim of the tensors (<= D: columns d..D-1 are zero-filled by TMA, never stored)
     float scale, scale_log2;
     int causal, window;
 };
@@ -450,8 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && n_it > 0) ok = wait_bar_warp(bar(B_ACC), 0, abort_flag, p.err);
         if (ok) {
             ptx::tc_fence_after();
-            T* dVrow = static_cast<T*>(p.dV) + ((size_t)bkv * p.S_k + j) * D;
-            T* dKrow = static_cast<T*>(p.dK) + ((size_t)bkv * p.S_k + j) * D;
+            T* dVrow = static_cast<T*>(p.dV) + ((size_t)bkv * p.S_k + j) * p.d;
+            T* dKrow = static_cast<T*>(p.dK) + ((size_t)bkv * p.S_k + j) * p.d;
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc) {
                 const int c = hf * (D / 64) + cc;  // 32-column chunk
@@ -473,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ov[k] = pack2<kBF16>(__uint_as_float(rv[e]), __uint_as_float(rv[e + 1]));
                         ok4[k] = pack2<kBF16>(__uint_as_float(rk[e]) * p.scale, __uint_as_float(rk[e + 1]) * p.scale);
                     }
-                    if (row_valid) {
+                    if (row_valid && c * 32 + u * 8 < p.d) {
                         *reinterpret_cast<uint4*>(dVrow + c * 32 + u * 8) = make_uint4(ov[0], ov[1], ov[2], ov[3]);
                         *reinterpret_cast<uint4*>(dKrow + c * 32 + u * 8) = make_uint4(ok4[0], ok4[1], ok4[2], ok4[3]);
                     }
@@ -557,9 +558,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int h = 0; h < D / 64; ++h) {  // one bulk group per staging area, dS tile first
                     const uint32_t area = sbase + (h == 0 ? C::OFF_DS : C::OFF_DO + s * C::kTileQ_B);
-                    if (go) {
-                        ptx::tma_reduce_add_3d(&tmdQ, area, h * 64, m0, bh);
-                        ptx::tma_reduce_add_3d(&tmdQ, area + BM * 128, h * 64 + 32, m0, bh);
+                    if (go) {  // 32-column boxes past the head dim hold zeros and are not added
+                        if (h * 64 < p.d) ptx::tma_reduce_add_3d(&tmdQ, area, h * 64, m0, bh);
+                        if (h * 64 + 32 < p.d) ptx::tma_reduce_add_3d(&tmdQ, area + BM * 128, h * 64 + 32, m0, bh);
                     }
                     ptx::bulk_commit_group();
                 }
@@ -641,9 +642,12 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, const void* dO
     CUtensorMap tq, tk, tv, tdo, tdq;
     const CUtensorMapDataType dt =
         TypeTraits<T>::kId == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    if (!make_map(&tq, Q, dt, 2, s.B * s.H, s.S_q, D) || !make_map(&tk, K, dt, 2, s.B * s.H_kv, s.S_k, D) ||
-        !make_map(&tv, V, dt, 2, s.B * s.H_kv, s.S_k, D) || !make_map(&tdo, dO, dt, 2, s.B * s.H, s.S_q, D) ||
-        !make_map(&tdq, ws.dqacc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s.B * s.H, s.S_q, D))
+    // global extents and strides use the tensors' head dim s.d; the kernel reads D columns
+    // (boxes past s.d come back zero-filled)
+    if (s.d > D || s.d % 32 != 0 || !make_map(&tq, Q, dt, 2, s.B * s.H, s.S_q, s.d) ||
+        !make_map(&tk, K, dt, 2, s.B * s.H_kv, s.S_k, s.d) || !make_map(&tv, V, dt, 2, s.B * s.H_kv, s.S_k, s.d) ||
+        !make_map(&tdo, dO, dt, 2, s.B * s.H, s.S_q, s.d) ||
+        !make_map(&tdq, ws.dqacc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s.B * s.H, s.S_q, s.d))
         return cudaErrorInvalidValue;
     Params p;
     p.lse2 = ws.lse2;
@@ -658,6 +662,7 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, const void* dO
     p.S_q = s.S_q;
     p.S_k = s.S_k;
     p.S_q_pad = s.S_q_pad;
+    p.d = s.d;
     p.scale = s.scale;
     p.scale_log2 = s.scale * 1.4426950408889634f;
     p.causal = s.causal;
@@ -675,10 +680,11 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, const void* dO
 cudaError_t launch_bwd_sm103(int dtype, const void* Q, const void* K, const void* V,
                              const void* dO, const Workspace& ws, void* dK, void* dV,
                              const Shape& s, cudaStream_t st) {
-    if (s.d == 64) {
+    const int D = tc_head_dim(s.d);  // d = 32 / 96 run the 64 / 128 kernels
+    if (D == 64) {
         if (dtype == FA_F16) return launch_t<__half, 64>(Q, K, V, dO, ws, dK, dV, s, st);
         if (dtype == FA_BF16) return launch_t<__nv_bfloat16, 64>(Q, K, V, dO, ws, dK, dV, s, st);
-    } else if (s.d == 128) {
+    } else if (D == 128) {
         if (dtype == FA_F16) return launch_t<__half, 128>(Q, K, V, dO, ws, dK, dV, s, st);
         if (dtype == FA_BF16) return launch_t<__nv_bfloat16, 128>(Q, K, V, dO, ws, dK, dV, s, st);
     }

@@ -93,6 +93,30 @@ __host__ __device__ __forceinline__ void key_range(const Shape& s, int i0, int i
     }
 }
 
+// Head dims the library takes.  The CUDA-core kernels and the preprocess are instantiated
+// for each; the tensor-core kernels run d = 32 and 96 as d = 64 and 128 with the missing
+// columns zero-filled by TMA (their global extents and strides stay d), d = 256 on CUDA cores.
+#define FA_FOR_DTYPE(dtype, DD, CALL)              \
+    do {                                           \
+        if ((dtype) == FA_F32) CALL(float, DD);    \
+        if ((dtype) == FA_F16) CALL(__half, DD);   \
+        if ((dtype) == FA_BF16) CALL(__nv_bfloat16, DD); \
+    } while (0)
+#define FA_DISPATCH_HEAD_DIM(dtype, d, CALL)                      \
+    do {                                                          \
+        switch (d) {                                              \
+            case 32: FA_FOR_DTYPE(dtype, 32, CALL); break;        \
+            case 64: FA_FOR_DTYPE(dtype, 64, CALL); break;        \
+            case 96: FA_FOR_DTYPE(dtype, 96, CALL); break;        \
+            case 128: FA_FOR_DTYPE(dtype, 128, CALL); break;      \
+            case 256: FA_FOR_DTYPE(dtype, 256, CALL); break;      \
+            default: break;                                       \
+        }                                                         \
+    } while (0)
+inline bool head_dim_supported(int d) { return d == 32 || d == 64 || d == 96 || d == 128 || d == 256; }
+// The tensor-core kernels' compiled head dim for a call's d (0: none, CUDA cores instead).
+inline int tc_head_dim(int d) { return d == 32 || d == 64 ? 64 : (d == 96 || d == 128 ? 128 : 0); }
+
 // Device error word codes (bit set by a kernel whose bounded wait ran out).
 enum : unsigned int {
     kErrTimeout = 1u,

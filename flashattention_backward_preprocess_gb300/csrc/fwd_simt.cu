@@ -154,15 +154,7 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, void* O, float
 cudaError_t launch_fwd_simt(int dtype, const void* Q, const void* K, const void* V, void* O,
                             float* LSE, const Shape& s, cudaStream_t st) {
 #define FA_L(T, DD) return launch_t<T, DD>(Q, K, V, O, LSE, s, st)
-    if (s.d == 64) {
-        if (dtype == FA_F32) FA_L(float, 64);
-        if (dtype == FA_F16) FA_L(__half, 64);
-        if (dtype == FA_BF16) FA_L(__nv_bfloat16, 64);
-    } else if (s.d == 128) {
-        if (dtype == FA_F32) FA_L(float, 128);
-        if (dtype == FA_F16) FA_L(__half, 128);
-        if (dtype == FA_BF16) FA_L(__nv_bfloat16, 128);
-    }
+    FA_DISPATCH_HEAD_DIM(dtype, s.d, FA_L);
 #undef FA_L
     return cudaErrorInvalidValue;
 }

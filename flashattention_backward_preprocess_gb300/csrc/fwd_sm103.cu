@@ -67,6 +67,7 @@ struct FParams {
     float* LSE;
     unsigned int* err;
     int B, H, H_kv, S_q, S_k;
+    int d;  // head dim of the tensors (<= D: columns d..D-1 are zero-filled by TMA, never stored)
     float scale_log2;
     int window;  // sliding-window size, 0 = none
 };
@@ -305,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
             ptx::tc_fence_after();
             const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-            T* Orow = static_cast<T*>(p.O) + ((size_t)bh * p.S_q + i) * D;
+            T* Orow = static_cast<T*>(p.O) + ((size_t)bh * p.S_q + i) * p.d;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -323,7 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = 0; k < 4; ++k)
                         w4[k] = pack2<kBF16>(__uint_as_float(o[u * 8 + 2 * k]) * inv_l,
                                              __uint_as_float(o[u * 8 + 2 * k + 1]) * inv_l);
-                    if (row_valid) *reinterpret_cast<uint4*>(Orow + c * 32 + u * 8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    if (row_valid && c * 32 + u * 8 < p.d)
+                        *reinterpret_cast<uint4*>(Orow + c * 32 + u * 8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
             }
             if (row_valid)
@@ -381,8 +383,9 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, void* O, float
     const CUtensorMapDataType dt =
         TypeTraits<T>::kId == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap tq, tk, tv;
-    if (!make_map(&tq, Q, dt, s.B * s.H, s.S_q, D) || !make_map(&tk, K, dt, s.B * s.H_kv, s.S_k, D) ||
-        !make_map(&tv, V, dt, s.B * s.H_kv, s.S_k, D))
+    // global extents and strides use the tensors' head dim s.d; the kernel reads D columns
+    if (s.d > D || s.d % 32 != 0 || !make_map(&tq, Q, dt, s.B * s.H, s.S_q, s.d) ||
+        !make_map(&tk, K, dt, s.B * s.H_kv, s.S_k, s.d) || !make_map(&tv, V, dt, s.B * s.H_kv, s.S_k, s.d))
         return cudaErrorInvalidValue;
     FParams p;
     p.O = O;
@@ -393,6 +396,7 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, void* O, float
     p.H_kv = s.H_kv;
     p.S_q = s.S_q;
     p.S_k = s.S_k;
+    p.d = s.d;
     p.scale_log2 = s.scale * 1.4426950408889634f;
     p.window = s.window;
     auto kern = fwd_sm103_kernel<T, D>;
@@ -407,10 +411,11 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, void* O, float
 
 cudaError_t launch_fwd_sm103(int dtype, const void* Q, const void* K, const void* V, void* O, float* LSE,
                             unsigned int* err, const Shape& s, cudaStream_t st) {
-    if (s.d == 64) {
+    const int D = tc_head_dim(s.d);  // d = 32 / 96 run the 64 / 128 kernels
+    if (D == 64) {
         if (dtype == FA_F16) return launch_t<__half, 64>(Q, K, V, O, LSE, err, s, st);
         if (dtype == FA_BF16) return launch_t<__nv_bfloat16, 64>(Q, K, V, O, LSE, err, s, st);
-    } else if (s.d == 128) {
+    } else if (D == 128) {
         if (dtype == FA_F16) return launch_t<__half, 128>(Q, K, V, O, LSE, err, s, st);
         if (dtype == FA_BF16) return launch_t<__nv_bfloat16, 128>(Q, K, V, O, LSE, err, s, st);
     }

@@ -4,8 +4,9 @@
 // Step 1 (boostr flash_bwd.rs, "Step 1: Preprocessing -- compute
 // D = rowsum(dO (.) O) per query position"): one fp32 dot product per query
 // row.  It is HBM-bound (2 * d * sizeof(T) bytes read per row), so the kernel
-// is a plain streaming row reduction: each thread loads one 16-byte chunk of
-// dO and of O, a group of d*sizeof(T)/16 lanes reduces a row with shuffles.
+// is a plain streaming row reduction: a group of LPR lanes (the row's 16-byte
+// chunks rounded up to a power of two, at most 32) loads the row's chunks of
+// dO and O, one or more per lane, and reduces with shuffles.
 // In the fused form used by fa_bwd the same pass also
 //   * writes LSE * log2(e) into a row-padded copy (so the main kernel can use
 //     exp2 and read whole 128-row tiles with one bulk copy; padding rows and
@@ -22,6 +23,13 @@
 namespace fa {
 namespace {
 
+// Lanes per row: the row's chunk count rounded up to a power of two, at most a warp.
+constexpr int lanes_per_row(int chunks) {
+    int l = 1;
+    while (l < chunks && l < 32) l *= 2;
+    return l;
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(256) preprocess_kernel(const T* __restrict__ dO,
                                                          const T* __restrict__ O,
@@ -31,8 +39,9 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const T* __restrict__ d
                                                          float* __restrict__ dqacc, int BH,
                                                          int S_q, int rows_stride) {
     constexpr int VEC = 16 / sizeof(T);  // elements per 16-byte chunk
-    constexpr int LPR = D / VEC;         // lanes per row (8, 16 or 32)
-    static_assert(LPR >= 1 && LPR <= 32 && (32 % LPR) == 0, "row must fit a warp");
+    constexpr int CPR = D / VEC;         // 16-byte chunks per row
+    constexpr int LPR = lanes_per_row(CPR);
+    static_assert(CPR * VEC == D && LPR >= 1 && LPR <= 32 && (32 % LPR) == 0, "row split");
     const long total_rows = (long)BH * rows_stride;
     const long gtid = (long)blockIdx.x * blockDim.x + threadIdx.x;
     const long row = gtid / LPR;        // padded row index (bh * rows_stride + i)
@@ -44,19 +53,21 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const T* __restrict__ d
 
     float acc = 0.f;
     if (valid) {
-        const size_t off = ((size_t)bh * S_q + i) * D + (size_t)lane_in_row * VEC;
-        const int4 a = __ldg(reinterpret_cast<const int4*>(dO + off));
-        const int4 b = __ldg(reinterpret_cast<const int4*>(O + off));
-        const T* ta = reinterpret_cast<const T*>(&a);
-        const T* tb = reinterpret_cast<const T*>(&b);
 #pragma unroll
-        for (int k = 0; k < VEC; ++k)
-            acc = fmaf(TypeTraits<T>::to_f32(ta[k]), TypeTraits<T>::to_f32(tb[k]), acc);
-        if (dqacc != nullptr) {
-            float4* z = reinterpret_cast<float4*>(dqacc + ((size_t)bh * S_q + i) * D +
-                                                  (size_t)lane_in_row * VEC);
+        for (int ch = lane_in_row; ch < CPR; ch += LPR) {
+            const size_t off = ((size_t)bh * S_q + i) * D + (size_t)ch * VEC;
+            const int4 a = __ldg(reinterpret_cast<const int4*>(dO + off));
+            const int4 b = __ldg(reinterpret_cast<const int4*>(O + off));
+            const T* ta = reinterpret_cast<const T*>(&a);
+            const T* tb = reinterpret_cast<const T*>(&b);
 #pragma unroll
-            for (int k = 0; k < VEC / 4; ++k) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int k = 0; k < VEC; ++k)
+                acc = fmaf(TypeTraits<T>::to_f32(ta[k]), TypeTraits<T>::to_f32(tb[k]), acc);
+            if (dqacc != nullptr) {
+                float4* z = reinterpret_cast<float4*>(dqacc + off);
+#pragma unroll
+                for (int k = 0; k < VEC / 4; ++k) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
     }
 #pragma unroll
@@ -99,7 +110,7 @@ template <typename T, int D>
 cudaError_t launch_pre_t(const void* dO, const void* O, const float* LSE, float* Dout,
                          float* lse2, float* dqacc, const Shape& s, int rows_stride,
                          cudaStream_t st) {
-    constexpr int LPR = D / (16 / sizeof(T));
+    constexpr int LPR = lanes_per_row(D / (16 / (int)sizeof(T)));
     const long threads = (long)s.B * s.H * rows_stride * LPR;
     const int block = 256;
     const long grid = (threads + block - 1) / block;
@@ -129,15 +140,7 @@ cudaError_t launch_preprocess(int dtype, const void* dO, const void* O, const fl
                               float* D, float* lse2, float* dqacc, const Shape& s,
                               int rows_stride, cudaStream_t st) {
 #define FA_PRE(T, DD) return launch_pre_t<T, DD>(dO, O, LSE, D, lse2, dqacc, s, rows_stride, st)
-    if (s.d == 64) {
-        if (dtype == FA_F32) FA_PRE(float, 64);
-        if (dtype == FA_F16) FA_PRE(__half, 64);
-        if (dtype == FA_BF16) FA_PRE(__nv_bfloat16, 64);
-    } else if (s.d == 128) {
-        if (dtype == FA_F32) FA_PRE(float, 128);
-        if (dtype == FA_F16) FA_PRE(__half, 128);
-        if (dtype == FA_BF16) FA_PRE(__nv_bfloat16, 128);
-    }
+    FA_DISPATCH_HEAD_DIM(dtype, s.d, FA_PRE);
 #undef FA_PRE
     return cudaErrorInvalidValue;
 }

@@ -58,7 +58,7 @@ typedef enum { FA_F32 = 0, FA_F16 = 1, FA_BF16 = 2 } fa_dtype;
 typedef enum {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = 1, /* bad pointer, shape, dtype, scale or alignment */
-    FA_ERR_UNSUPPORTED = 2, /* valid but not implemented (head dim not 64 / 128) */
+    FA_ERR_UNSUPPORTED = 2, /* valid but not implemented (head dim not 32/64/96/128/256) */
     FA_ERR_CUDA = 3,        /* a CUDA runtime / driver call failed */
     FA_ERR_TIMEOUT = 4,     /* a device-side bounded wait ran out */
     FA_ERR_NOMEM = 5        /* workspace allocation failed */
@@ -71,12 +71,15 @@ typedef enum {
  *   LSE           : [B, H, S_q] float32, 4-byte aligned
  *   dQ            : [B, H, S_q, d]  dtype, written
  *   dK, dV        : [B, H_kv, S_k, d] dtype, written (rows no query sees get 0)
- *   B, H, H_kv, S_q, S_k > 0, H % H_kv == 0, d in {64, 128}
+ *   B, H, H_kv, S_q, S_k > 0, H % H_kv == 0, d in {32, 64, 96, 128, 256}
  *   scale         : finite, > 0 (usually 1/sqrt(d))
  *   causal        : 0 or 1
  *   dtype         : fa_dtype (F32, F16, BF16); accumulation is fp32
  *   stream        : cudaStream_t
- * F16/BF16 run the tcgen05 tensor-core kernel; F32 runs an FFMA kernel.
+ * F16/BF16 with d <= 128 run the tcgen05 tensor-core kernel (d = 32 and 96
+ * on the d = 64 and 128 kernels, the missing columns read as zeros); F32 and
+ * d = 256 (whose dK and dV alone would fill the 512 TMEM columns) run FFMA
+ * kernels.
  * dQ is reduced across key tiles with fp32 atomics, so dQ may differ in the
  * last bits between runs (flash_bwd.rs, "dQ must be zeroed -- backward uses
  * atomicAdd"); dK and dV are deterministic.  fa_bwd_ex(..., deterministic = 1)
@@ -102,8 +105,9 @@ int fa_bwd_preprocess(const void* dO, const void* O, float* D, int B, int H, int
  * LSE_i = log sum_j exp(scale <Q_i, K_j>) over the visible keys.
  *   Q : [B, H, S_q, d], K, V : [B, H_kv, S_k, d], O : [B, H, S_q, d] dtype;
  *   LSE : [B, H, S_q] float32.  Rows that see no key get O = 0, LSE = -inf.
- * F16/BF16 with d in {64, 128} run a tcgen05 tensor-core kernel (fp32
- * accumulation, online softmax over 128-key tiles); F32 runs an FFMA kernel.
+ * F16/BF16 with d <= 128 run a tcgen05 tensor-core kernel (fp32
+ * accumulation, online softmax over 128-key tiles); F32 and d = 256 run an
+ * FFMA kernel.
  */
 int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
            int H_kv, int S_q, int S_k, int d, float scale, int causal, int dtype, void* stream);

@@ -67,8 +67,8 @@ def _bwd(lib, **kw):
     (dict(S_q=0), 1, "S_q"),
     (dict(S_k=-3), 1, "S_k"),
     (dict(dtype=7), 1, "dtype"),
-    (dict(d=96), 2, "d"),
-    (dict(d=256), 2, "d"),
+    (dict(d=80), 2, "d"),
+    (dict(d=512), 2, "d"),
     (dict(scale=0.0), 1, "scale"),
     (dict(scale=float("nan")), 1, "scale"),
     (dict(scale=-1.0), 1, "scale"),
@@ -135,4 +135,4 @@ def test_ex_entry_points_validate(lib):
     f = [P[0], P[1], P[2], P[3], P[4], 1, 4, 4, 8, 8, 64, 0.1, 0]
     assert lib.fa_fwd_ex(*f, -5, fa.FA_BF16, None) == 1
     assert fa.fa_last_error().startswith("window_size:")
-    assert lib.fa_fwd_ex(*f[:10], 96, 0.1, 0, 3, fa.FA_BF16, None) == 2
+    assert lib.fa_fwd_ex(*f[:10], 80, 0.1, 0, 3, fa.FA_BF16, None) == 2

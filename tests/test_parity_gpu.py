@@ -332,3 +332,44 @@ def test_deterministic_dq_bench_workload_bitwise():
     qrows = sample_rows(w.B * w.H, w.S_q, 128, np.random.default_rng(3))
     ref = oracle.ref_dq_rows(*args, qrows, w.scale, True)
     assert rel_err(f64(a[0]).reshape(-1, w.d)[qrows], ref) <= TOL[w.dtype]
+
+
+HEAD_DIMS = [
+    # dtype, B, H, H_kv, S_q, S_k, d, causal, window, deterministic
+    ("bf16", 1, 4, 2, 300, 300, 96, True, 0, False),    # tensor cores, 128-wide kernel, 32 zero columns
+    ("f16", 1, 4, 4, 257, 129, 96, False, 0, False),
+    ("bf16", 1, 4, 1, 260, 260, 32, True, 0, False),    # tensor cores, 64-wide kernel
+    ("f16", 2, 2, 2, 130, 390, 32, False, 100, False),  # + window
+    ("bf16", 1, 4, 2, 333, 333, 96, True, 0, True),     # + deterministic dQ
+    ("bf16", 1, 2, 1, 200, 200, 256, True, 0, False),   # d = 256: CUDA-core kernels
+    ("f16", 1, 2, 2, 130, 70, 256, False, 0, True),
+    ("f32", 1, 2, 1, 150, 150, 96, True, 0, False),
+    ("f32", 1, 2, 2, 100, 160, 32, False, 30, True),
+    ("f32", 1, 2, 1, 90, 90, 256, True, 0, False),
+]
+
+
+@pytest.mark.parametrize("case", HEAD_DIMS, ids=lambda c: "-".join(map(str, c)))
+def test_head_dims_forward_and_backward(case):
+    dt, B, H, H_kv, S_q, S_k, d, causal, win, det = case
+    w = Workload("hd", dt, B, H, H_kv, S_q, S_k, d, causal, seed=61, window=win)
+    Q, K, V, dO = (x.cuda() for x in make_inputs(w))
+    O, LSE = fa.fa_fwd(Q, K, V, scale=w.scale, causal=causal, window_size=win)
+    torch.cuda.synchronize()
+    fa.fa_check_device()
+    O64, L64 = oracle.ref_fwd(f64(Q), f64(K), f64(V), w.scale, causal, win)
+    assert rel_err(f64(O), O64) <= TOL[dt]
+    fin = np.isfinite(L64)
+    assert float(np.max(np.abs(f64(LSE)[fin] - L64[fin]))) <= 1e-4
+    if dt == "f32":  # the backward gate isolates the backward: fp32 O / LSE from the oracle
+        O = torch.from_numpy(O64).float().cuda()
+        LSE = torch.from_numpy(L64).float().cuda()
+    dQ, dK, dV = fa.fa_bwd(dO, Q, K, V, O, LSE, scale=w.scale, causal=causal, window_size=win,
+                           deterministic=det)
+    torch.cuda.synchronize()
+    fa.fa_check_device()
+    ref = oracle.ref_bwd(f64(dO), f64(Q), f64(K), f64(V), f64(O), f64(LSE), w.scale, causal, win)
+    for name, got, r in zip(("dQ", "dK", "dV"), (dQ, dK, dV), ref[:3]):
+        g = f64(got)
+        assert np.all(np.isfinite(g)), name
+        assert rel_err(g, r) <= TOL[dt], (name, rel_err(g, r))
