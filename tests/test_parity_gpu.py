@@ -373,3 +373,39 @@ def test_head_dims_forward_and_backward(case):
         g = f64(got)
         assert np.all(np.isfinite(g)), name
         assert rel_err(g, r) <= TOL[dt], (name, rel_err(g, r))
+
+
+@pytest.mark.parametrize("det", [False, True])
+def test_backward_captures_into_a_cuda_graph(det):
+    # after one call on a stream (which caches that stream's workspace) fa_bwd enqueues
+    # kernels and, in deterministic mode, one memset, and nothing else: it can be captured
+    # into a CUDA graph, and replays on new input values match direct calls
+    w = Workload("graph", "bf16", 2, 8, 2, 700, 700, 128, True, seed=71)
+    Q, K, V, dO, O, LSE = prepare(w)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fa.fa_bwd(dO, Q, K, V, O, LSE, causal=True, dQ=dQ, dK=dK, dV=dV, deterministic=det)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fa.fa_bwd(dO, Q, K, V, O, LSE, causal=True, dQ=dQ, dK=dK, dV=dV, deterministic=det)
+    for seed in (72, 73):
+        Qn, Kn, Vn, dOn = make_inputs(w.with_(seed=seed))
+        for dst, src in zip((Q, K, V, dO), (Qn, Kn, Vn, dOn)):
+            dst.copy_(src)
+        On, Ln = fa.fa_fwd(Q, K, V, causal=True)
+        O.copy_(On)
+        LSE.copy_(Ln)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        fa.fa_check_device()
+        ref = fa.fa_bwd(dO, Q, K, V, O, LSE, causal=True, deterministic=det)
+        torch.cuda.synchronize()
+        assert torch.equal(dK, ref[1]) and torch.equal(dV, ref[2])
+        if det:
+            assert torch.equal(dQ, ref[0])
+        else:
+            assert rel_err(f64(dQ), f64(ref[0])) < 1e-2
