@@ -72,6 +72,13 @@ struct FParams {
     int window;  // sliding-window size, 0 = none
 };
 
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 template <bool kBF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     if (kBF16) {
@@ -245,21 +252,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c) ptx::tmem_ld32p(buf + c * 32, r + c * 32);
             ptx::tmem_wait_ld();
-            float x[BN];
-            float mx = -INFINITY;
+            // masked scores become -inf in place; row max over eight independent chains of
+            // three-input maxima (one instruction per two scores)
             if (masked) {
 #pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    x[c] = (unsigned)(c - c_lo) < c_span ? __uint_as_float(r[c]) * p.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, x[c]);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    x[c] = __uint_as_float(r[c]) * p.scale_log2;
-                    mx = fmaxf(mx, x[c]);
-                }
+                for (int c = 0; c < BN; ++c)
+                    r[c] = (unsigned)(c - c_lo) < c_span ? r[c] : __float_as_uint(-INFINITY);
             }
+            float mx8[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) mx8[q] = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < BN; c += 2)
+                mx8[(c >> 1) & 7] = fmax3(mx8[(c >> 1) & 7], __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+            float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            mx = mx == -INFINITY ? -INFINITY : mx * p.scale_log2;
             // lazy running max: move it only when this tile exceeds it by more than the margin
             float alpha = 1.f;
             const bool rescale = mx > m_run + kRescaleLog2;
@@ -268,14 +276,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_run = mx;
             }
             const float m_use = m_run == -INFINITY ? 0.f : m_run;  // rows with nothing visible yet: P = 0
-            float sum = 0.f;
+            // scale-and-shift and the row sum on packed fp32 pairs (one instruction per two
+            // scores); -inf scores give P = 0
+            const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+            const float2 nm2 = make_float2(-m_use, -m_use);
+            float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                              make_float2(0.f, 0.f)};
             uint32_t Pp[BN / 2];
 #pragma unroll
             for (int c = 0; c < BN; c += 2) {
-                const float p0 = ptx::ex2(x[c] - m_use), p1 = ptx::ex2(x[c + 1] - m_use);
-                sum += p0 + p1;
-                Pp[c / 2] = pack2<kBF16>(p0, p1);
+                const float2 x = __ffma2_rn(make_float2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])), sc2, nm2);
+                const float2 pp = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+                sum2[(c >> 1) & 3] = __fadd2_rn(sum2[(c >> 1) & 3], pp);
+                Pp[c / 2] = pack2<kBF16>(pp.x, pp.y);
             }
+            const float2 s2 = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
+            const float sum = s2.x + s2.y;
             l_run = l_run * alpha + sum;
             ptx::tmem_st32(buf, Pp);  // packed P into columns [0, 64): already read
             ptx::tmem_st32(buf + 32, Pp + 32);
