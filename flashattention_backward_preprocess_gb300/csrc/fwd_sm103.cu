@@ -35,8 +35,8 @@ namespace {
 
 constexpr int BM = 128;  // query rows per CTA
 constexpr int BN = 128;  // key rows per step
-constexpr int kThreads = 192;
-constexpr int kWarpTma = 4, kWarpMma = 5;
+constexpr int kThreads = 224;
+constexpr int kWarpTma = 4, kWarpMma = 5, kWarpPv = 6;  // MMA issuers: S products (5), P V products (6)
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;  // move the running max only past this margin
 
@@ -57,8 +57,8 @@ enum {
     F_Q = 0,      // Q tile landed (TMA)
     F_S0,         // S(j) in buffer j % 2 (MMA commit), two slots
     F_P0 = F_S0 + 2,  // P(j) packed in buffer j % 2 (4 softmax warps), two slots
-    F_PV = F_P0 + 2,  // O += P(j) V(j) done (MMA commit)
-    F_FINAL,      // MMA shutdown
+    F_PV0 = F_P0 + 2, // O += P(j) V(j) done (MMA commit), one slot per S buffer j % 2
+    F_FINAL = F_PV0 + 2,  // every product done (P V issuer's last commit)
     F_STAGE0      // then STAGES "full" barriers, then STAGES "empty" barriers
 };
 
@@ -174,55 +174,60 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = issued - C::STAGES < 0 ? 0 : issued - C::STAGES; j < issued; ++j)
                 drain_wait(bar_full(j % C::STAGES), (j / C::STAGES) & 1);
         }
-    } else if (warp == kWarpMma) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == kWarpMma || warp == kWarpPv) {
+        // ------------------------------------------------------------ MMA issuers
+        // tcgen05.mma issue stalls while the tensor pipe's short queue is full, so one thread
+        // can run only about one product ahead of the pipe and every commit, barrier wait and
+        // fence it executes leaves the pipe idle.  Two issuers hide each other's bookkeeping:
+        // warp 5 issues S = Q K^T, warp 6 issues O += P V.  Products of different threads are
+        // not ordered with each other, so every hazard between them goes through a barrier:
+        // S(j) into buffer j % 2 waits until P V(j-2) has read P out of it (one P V barrier per
+        // buffer, so that wait can never see a phase two ahead), and P V(j) runs only once the
+        // softmax has turned S(j) into P(j), which implies S(j) is complete.
         if (lane == 0 && !*abort_flag && n_cnt > 0) {
             constexpr uint32_t ID_S = ptx::idesc_f16(BM, BN, kBF16, false, false);  // S = Q K^T
             constexpr uint32_t ID_PV = ptx::idesc_f16(BM, D, kBF16, false, true);   // O += P V (A in TMEM)
             auto desc_add = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
-            const uint64_t dQ_k = ptx::sw128_desc(sbase + C::OFF_Q, 16, 1024);
-            const uint64_t dK_k = ptx::sw128_desc(sbase + C::OFF_K, 16, 1024);          // + stage offset
-            const uint64_t dV_mn = ptx::sw128_desc(sbase + C::OFF_V, C::kBox_B, 1024);  // + stage offset
-            // S(j) = Q K(j)^T into buffer j % 2 (both operands K-major)
-            auto gemm_s = [&](int j) {
-                const uint32_t so = (uint32_t)(j % C::STAGES) * C::kTile_B;
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t ko = (k / 4) * C::kBox_B + (k % 4) * 32;
-                    ptx::mma_ss(tmem + C::TM_S + (j & 1) * 128, desc_add(dQ_k, ko), desc_add(dK_k, so + ko), ID_S,
-                                k > 0);
-                }
-                ptx::mma_commit(bar(F_S0 + (j & 1)));
-            };
-            bool ok = wait_bar(bar(F_Q), 0, abort_flag, p.err);
-            for (int j = 0; ok && j < 2 && j < n_cnt; ++j) {
-                if (!(ok = wait_bar(bar_full(j % C::STAGES), (j / C::STAGES) & 1, abort_flag, p.err))) break;
-                ptx::tc_fence_after();
-                gemm_s(j);
-            }
-            for (int j = 0; ok && j < n_cnt; ++j) {
-                const int s = j % C::STAGES;
-                // O += P(j) V(j)   (A = P packed in buffer j % 2: 16 keys = 8 packed columns per step)
-                if (!(ok = wait_bar(bar(F_P0 + (j & 1)), (j >> 1) & 1, abort_flag, p.err))) break;
-                ptx::tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < BN / 16; ++k)
-                    ptx::mma_ts(tmem + C::TM_O, tmem + C::TM_S + (j & 1) * 128 + k * 8,
-                                desc_add(dV_mn, (uint32_t)s * C::kTile_B + k * 2048), ID_PV, (j > 0 || k > 0) ? 1u : 0u);
-                ptx::mma_commit(bar(F_PV));
-                ptx::mma_commit(bar_empty(s));  // K(j), V(j) no longer read
-                if (j + 2 < n_cnt) {
-                    // S(j+2) into buffer j % 2 once the P V product has read P(j) out of it
-                    const int s2 = (j + 2) % C::STAGES;
-                    if (!(ok = wait_bar(bar_full(s2), ((j + 2) / C::STAGES) & 1, abort_flag, p.err))) break;
-                    if (!(ok = wait_bar(bar(F_PV), j & 1, abort_flag, p.err))) break;
+            bool ok = true;
+            if (warp == kWarpMma) {
+                const uint64_t dQ_k = ptx::sw128_desc(sbase + C::OFF_Q, 16, 1024);
+                const uint64_t dK_k = ptx::sw128_desc(sbase + C::OFF_K, 16, 1024);  // + stage offset
+                ok = wait_bar(bar(F_Q), 0, abort_flag, p.err);
+                for (int j = 0; ok && j < n_cnt; ++j) {
+                    const int s = j % C::STAGES;
+                    if (!(ok = wait_bar(bar_full(s), (j / C::STAGES) & 1, abort_flag, p.err))) break;
+                    if (j >= 2 && !(ok = wait_bar(bar(F_PV0 + (j & 1)), ((j >> 1) - 1) & 1, abort_flag, p.err))) break;
                     ptx::tc_fence_after();
-                    gemm_s(j + 2);
+                    const uint32_t so = (uint32_t)s * C::kTile_B;
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t ko = (k / 4) * C::kBox_B + (k % 4) * 32;
+                        ptx::mma_ss(tmem + C::TM_S + (j & 1) * 128, desc_add(dQ_k, ko), desc_add(dK_k, so + ko), ID_S,
+                                    k > 0);
+                    }
+                    ptx::mma_commit(bar(F_S0 + (j & 1)));
                 }
+                // this thread's products must be complete before TMEM is released; every S it
+                // issued is read by a P V product, so they are, once the P V issuer drained
+            } else {
+                const uint64_t dV_mn = ptx::sw128_desc(sbase + C::OFF_V, C::kBox_B, 1024);  // + stage offset
+                for (int j = 0; ok && j < n_cnt; ++j) {
+                    const int s = j % C::STAGES;
+                    // O += P(j) V(j)   (A = P packed in buffer j % 2: 16 keys = 8 packed columns per step)
+                    if (!(ok = wait_bar(bar(F_P0 + (j & 1)), (j >> 1) & 1, abort_flag, p.err))) break;
+                    ptx::tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < BN / 16; ++k)
+                        ptx::mma_ts(tmem + C::TM_O, tmem + C::TM_S + (j & 1) * 128 + k * 8,
+                                    desc_add(dV_mn, (uint32_t)s * C::kTile_B + k * 2048), ID_PV,
+                                    (j > 0 || k > 0) ? 1u : 0u);
+                    ptx::mma_commit(bar(F_PV0 + (j & 1)));
+                    ptx::mma_commit(bar_empty(s));  // K(j), V(j) no longer read (S(j) completed before P(j))
+                }
+                // no MMA may still write TMEM when it is released
+                ptx::mma_commit(bar(F_FINAL));
+                drain_wait(bar(F_FINAL), 0);
             }
-            // no MMA may still write TMEM when it is released
-            ptx::mma_commit(bar(F_FINAL));
-            drain_wait(bar(F_FINAL), 0);
         }
         __syncwarp();
     } else {
@@ -297,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_st32(buf + 32, Pp + 32);
             // rescale the O row before the next P V product accumulates into it
             if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-                if (!(ok = wait_bar_warp(bar(F_PV), (j - 1) & 1, abort_flag, p.err))) break;
+                if (!(ok = wait_bar_warp(bar(F_PV0 + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag, p.err))) break;
                 ptx::tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
