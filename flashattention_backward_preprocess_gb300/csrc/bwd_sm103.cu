@@ -559,8 +559,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int h = 0; h < D / 64; ++h) {  // one bulk group per staging area, dS tile first
                     const uint32_t area = sbase + (h == 0 ? C::OFF_DS : C::OFF_DO + s * C::kTileQ_B);
                     if (go) {  // 32-column boxes past the head dim hold zeros and are not added
-                        if (h * 64 < p.d) ptx::tma_reduce_add_3d(&tmdQ, area, h * 64, m0, bh);
-                        if (h * 64 + 32 < p.d) ptx::tma_reduce_add_3d(&tmdQ, area + BM * 128, h * 64 + 32, m0, bh);
+                        // the accumulator lines stay in L2 ahead of the Q / dO stream: the
+                        // finalise pass then reads much of dQacc from L2
+                        const uint64_t pol = ptx::policy_evict_last();
+                        if (h * 64 < p.d) ptx::tma_reduce_add_3d_hint(&tmdQ, area, h * 64, m0, bh, pol);
+                        if (h * 64 + 32 < p.d) ptx::tma_reduce_add_3d_hint(&tmdQ, area + BM * 128, h * 64 + 32, m0, bh, pol);
                     }
                     ptx::bulk_commit_group();
                 }
