@@ -12,9 +12,9 @@
 //   * one CTA per (128-row query tile, query head); the query tiles with the most
 //     visible key tiles start first;
 //   * S = Q K^T for key tile j runs on the 5th-generation tensor cores into one of
-//     two 128-column TMEM buffers, so S(j+1) is computed while the softmax warps
-//     work on S(j); P = exp2(x - m) is packed to 16 bits in place and is the TMEM
-//     A operand of O += P V (O accumulates in TMEM, fp32);
+//     three 128-column TMEM buffers, so S(j+1) and S(j+2) are computed while the
+//     softmax warps work on S(j); P = exp2(x - m) is packed to 16 bits in place and
+//     is the TMEM A operand of O += P V (O accumulates in TMEM, fp32);
 //   * one softmax thread per query row (TMEM lane), logits handled in log2 units
 //     x = s * log2(e).  The running max m moves only when a tile's max exceeds it
 //     by more than 8 (P then stays <= 2^8); only then is the O row rescaled in
@@ -22,8 +22,9 @@
 //   * TMA (128-byte swizzle) loads the Q tile once and K / V through a ring;
 //     the epilogue divides O by the row sum and writes O and LSE;
 //   * warp roles: warps 0-3 softmax and epilogue, warp 4 TMA, warp 5 TMEM owner and
-//     MMA issuer; every mbarrier wait is bounded (a timeout records an error word,
-//     the other roles drop out, TMEM is freed and the kernel returns).
+//     issuer of the S products, warp 6 issuer of the P V products; every mbarrier wait
+//     is bounded (a timeout records an error word, the other roles drop out, TMEM is
+//     freed and the kernel returns).
 #include <math.h>
 
 #include "bounded_wait.cuh"
@@ -50,15 +51,16 @@ struct FCfg {
     static constexpr uint32_t OFF_K = OFF_Q + kTile_B;
     static constexpr uint32_t OFF_V = OFF_K + STAGES * kTile_B;
     static constexpr uint32_t OFF_BAR = OFF_V + STAGES * kTile_B;
-    static constexpr uint32_t TM_S = 0, TM_O = 256;     // S buffers [0,128), [128,256); O [256, 256+D)
+    // three S buffers [0,128), [128,256), [256,384); O [384, 384+D)
+    static constexpr uint32_t TM_S = 0, TM_O = 384;
 };
 
 enum {
     F_Q = 0,      // Q tile landed (TMA)
-    F_S0,         // S(j) in buffer j % 2 (MMA commit), two slots
-    F_P0 = F_S0 + 2,  // P(j) packed in buffer j % 2 (4 softmax warps), two slots
-    F_PV0 = F_P0 + 2, // O += P(j) V(j) done (MMA commit), one slot per S buffer j % 2
-    F_FINAL = F_PV0 + 2,  // every product done (P V issuer's last commit)
+    F_S0,             // S(j) in buffer j % 3 (MMA commit), one slot per buffer
+    F_P0 = F_S0 + 3,  // P(j) packed in buffer j % 3 (4 softmax warps), one slot per buffer
+    F_PV0 = F_P0 + 3, // O += P(j) V(j) done (MMA commit), one slot per buffer
+    F_FINAL = F_PV0 + 3,  // every product done (P V issuer's last commit)
     F_STAGE0      // then STAGES "full" barriers, then STAGES "empty" barriers
 };
 
@@ -135,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         if ((sbase & 1023u) != 0) atomicOr(p.err, kErrSmemAlign);
         *abort_flag = (sbase & 1023u) != 0;
-        for (int i = 0; i < kNumBars; ++i) ptx::mbar_init(bar(i), (i == F_P0 || i == F_P0 + 1) ? 4u : 1u);
+        for (int i = 0; i < kNumBars; ++i) ptx::mbar_init(bar(i), (i >= F_P0 && i < F_P0 + 3) ? 4u : 1u);
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
     }
@@ -181,9 +183,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // fence it executes leaves the pipe idle.  Two issuers hide each other's bookkeeping:
         // warp 5 issues S = Q K^T, warp 6 issues O += P V.  Products of different threads are
         // not ordered with each other, so every hazard between them goes through a barrier:
-        // S(j) into buffer j % 2 waits until P V(j-2) has read P out of it (one P V barrier per
+        // S(j) into buffer j % 3 waits until P V(j-3) has read P out of it (one P V barrier per
         // buffer, so that wait can never see a phase two ahead), and P V(j) runs only once the
-        // softmax has turned S(j) into P(j), which implies S(j) is complete.
+        // softmax has turned S(j) into P(j), which implies S(j) is complete.  Three S buffers let
+        // S(j+2) run while the softmax still works on S(j) and S(j+1).
         if (lane == 0 && !*abort_flag && n_cnt > 0) {
             constexpr uint32_t ID_S = ptx::idesc_f16(BM, BN, kBF16, false, false);  // S = Q K^T
             constexpr uint32_t ID_PV = ptx::idesc_f16(BM, D, kBF16, false, true);   // O += P V (A in TMEM)
@@ -196,16 +199,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; ok && j < n_cnt; ++j) {
                     const int s = j % C::STAGES;
                     if (!(ok = wait_bar(bar_full(s), (j / C::STAGES) & 1, abort_flag, p.err))) break;
-                    if (j >= 2 && !(ok = wait_bar(bar(F_PV0 + (j & 1)), ((j >> 1) - 1) & 1, abort_flag, p.err))) break;
+                    if (j >= 3 && !(ok = wait_bar(bar(F_PV0 + j % 3), (j / 3 - 1) & 1, abort_flag, p.err))) break;
                     ptx::tc_fence_after();
                     const uint32_t so = (uint32_t)s * C::kTile_B;
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
                         const uint32_t ko = (k / 4) * C::kBox_B + (k % 4) * 32;
-                        ptx::mma_ss(tmem + C::TM_S + (j & 1) * 128, desc_add(dQ_k, ko), desc_add(dK_k, so + ko), ID_S,
+                        ptx::mma_ss(tmem + C::TM_S + (j % 3) * 128, desc_add(dQ_k, ko), desc_add(dK_k, so + ko), ID_S,
                                     k > 0);
                     }
-                    ptx::mma_commit(bar(F_S0 + (j & 1)));
+                    ptx::mma_commit(bar(F_S0 + j % 3));
                 }
                 // this thread's products must be complete before TMEM is released; every S it
                 // issued is read by a P V product, so they are, once the P V issuer drained
@@ -213,15 +216,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t dV_mn = ptx::sw128_desc(sbase + C::OFF_V, C::kBox_B, 1024);  // + stage offset
                 for (int j = 0; ok && j < n_cnt; ++j) {
                     const int s = j % C::STAGES;
-                    // O += P(j) V(j)   (A = P packed in buffer j % 2: 16 keys = 8 packed columns per step)
-                    if (!(ok = wait_bar(bar(F_P0 + (j & 1)), (j >> 1) & 1, abort_flag, p.err))) break;
+                    // O += P(j) V(j)   (A = P packed in buffer j % 3: 16 keys = 8 packed columns per step)
+                    if (!(ok = wait_bar(bar(F_P0 + j % 3), (j / 3) & 1, abort_flag, p.err))) break;
                     ptx::tc_fence_after();
 #pragma unroll
                     for (int k = 0; k < BN / 16; ++k)
-                        ptx::mma_ts(tmem + C::TM_O, tmem + C::TM_S + (j & 1) * 128 + k * 8,
+                        ptx::mma_ts(tmem + C::TM_O, tmem + C::TM_S + (j % 3) * 128 + k * 8,
                                     desc_add(dV_mn, (uint32_t)s * C::kTile_B + k * 2048), ID_PV,
                                     (j > 0 || k > 0) ? 1u : 0u);
-                    ptx::mma_commit(bar(F_PV0 + (j & 1)));
+                    ptx::mma_commit(bar(F_PV0 + j % 3));
                     ptx::mma_commit(bar_empty(s));  // K(j), V(j) no longer read (S(j) completed before P(j))
                 }
                 // no MMA may still write TMEM when it is released
@@ -240,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float l_run = 0.f;        // sum of exp2(x - m_run)
         bool ok = !*abort_flag;
         for (int j = 0; ok && j < n_cnt; ++j) {
-            const uint32_t buf = tmem + C::TM_S + (j & 1) * 128 + lane_off;
+            const uint32_t buf = tmem + C::TM_S + (j % 3) * 128 + lane_off;
             const int n0 = (n_first + j) * BN;
             // Key columns c of this tile (key n0 + c) that the row sees form one interval
             // (visible_keys of the row's key position i + off), cut to the keys that exist.
@@ -251,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const unsigned c_span = c_hi > c_lo ? (unsigned)(c_hi - c_lo) : 0u;
             // warp-uniform: the chosen path holds .sync.aligned TMEM accesses
             const bool masked = __any_sync(0xffffffffu, !(c_lo <= 0 && c_hi >= BN));
-            if (!(ok = wait_bar_warp(bar(F_S0 + (j & 1)), (j >> 1) & 1, abort_flag, p.err))) break;
+            if (!(ok = wait_bar_warp(bar(F_S0 + j % 3), (j / 3) & 1, abort_flag, p.err))) break;
             ptx::tc_fence_after();
             uint32_t r[BN];
 #pragma unroll
@@ -302,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_st32(buf + 32, Pp + 32);
             // rescale the O row before the next P V product accumulates into it
             if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-                if (!(ok = wait_bar_warp(bar(F_PV0 + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag, p.err))) break;
+                if (!(ok = wait_bar_warp(bar(F_PV0 + (j - 1) % 3), ((j - 1) / 3) & 1, abort_flag, p.err))) break;
                 ptx::tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -317,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(F_P0 + (j & 1)));
+            if (lane == 0) ptx::mbar_arrive(bar(F_P0 + j % 3));
         }
         // ---- epilogue: O = acc / l, LSE = (m + log2 l) * ln 2.  Wait for the MMA issuer's
         // final commit (every product done), not for a parity of the shared P V barrier:
