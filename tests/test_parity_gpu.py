@@ -409,3 +409,51 @@ def test_backward_captures_into_a_cuda_graph(det):
             assert torch.equal(dQ, ref[0])
         else:
             assert rel_err(f64(dQ), f64(ref[0])) < 1e-2
+
+
+def _random_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        dt = str(rng.choice(["bf16", "f16", "f32"], p=[0.45, 0.35, 0.2]))
+        d = int(rng.choice([32, 64, 96, 128, 256], p=[0.15, 0.3, 0.15, 0.3, 0.1]))
+        H_kv = int(rng.integers(1, 3))
+        g = int(rng.choice([1, 2, 4]))
+        S_q = int(rng.integers(1, 450))
+        S_k = int(rng.integers(1, 450))
+        causal = bool(rng.integers(0, 2))
+        win = int(rng.choice([0, 0, int(rng.integers(1, 300))]))
+        det = bool(rng.integers(0, 2))
+        cases.append((dt, 1, g * H_kv, H_kv, S_q, S_k, d, causal, win, det))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_cases(30, 2026), ids=lambda c: "-".join(map(str, c)))
+def test_random_configurations(case):
+    """Seeded random draws over the whole option space (dtype, head dim, GQA ratio, ragged S_q
+    and S_k in either order, causal, window, deterministic): forward and backward against the
+    oracle."""
+    dt, B, H, H_kv, S_q, S_k, d, causal, win, det = case
+    w = Workload("rand", dt, B, H, H_kv, S_q, S_k, d, causal, seed=S_q * 1000 + S_k, window=win)
+    Q, K, V, dO = (x.cuda() for x in make_inputs(w))
+    O, LSE = fa.fa_fwd(Q, K, V, scale=w.scale, causal=causal, window_size=win)
+    torch.cuda.synchronize()
+    fa.fa_check_device()
+    O64, L64 = oracle.ref_fwd(f64(Q), f64(K), f64(V), w.scale, causal, win)
+    assert rel_err(f64(O), O64) <= TOL[dt]
+    lse, fin = f64(LSE), np.isfinite(L64)
+    assert bool(np.all(np.isneginf(lse[~fin])))
+    if fin.any():
+        assert float(np.max(np.abs(lse[fin] - L64[fin]))) <= 1e-4
+    if dt == "f32":
+        O = torch.from_numpy(O64).float().cuda()
+        LSE = torch.from_numpy(L64).float().cuda()
+    dQ, dK, dV = fa.fa_bwd(dO, Q, K, V, O, LSE, scale=w.scale, causal=causal, window_size=win,
+                           deterministic=det)
+    torch.cuda.synchronize()
+    fa.fa_check_device()
+    ref = oracle.ref_bwd(f64(dO), f64(Q), f64(K), f64(V), f64(O), f64(LSE), w.scale, causal, win)
+    for name, got, r in zip(("dQ", "dK", "dV"), (dQ, dK, dV), ref[:3]):
+        g_ = f64(got)
+        assert np.all(np.isfinite(g_)), name
+        assert rel_err(g_, r) <= TOL[dt], (name, rel_err(g_, r))
