@@ -280,7 +280,7 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
         return rc;
     const Shape s = make_shape(B, H, H_kv, S_q, S_k, d, scale, causal, window);
     cudaError_t e;
-    if (dtype == FA_F32 || fwd_simt_for_16bit() || tc_head_dim(d) == 0) {
+    if (dtype == FA_F32 || fwd_simt_for_16bit()) {
         e = launch_fwd_simt(dtype, Q, K, V, O, LSE, s, st);
     } else {
         // the tensor-core forward reports bounded-wait timeouts in the stream's workspace

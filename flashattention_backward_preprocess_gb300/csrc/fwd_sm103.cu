@@ -35,7 +35,6 @@ namespace fa {
 namespace {
 
 constexpr int BM = 128;  // query rows per CTA
-constexpr int BN = 128;  // key rows per step
 constexpr int kThreads = 224;
 constexpr int kWarpTma = 4, kWarpMma = 5, kWarpPv = 6;  // MMA issuers: S products (5), P V products (6)
 constexpr uint32_t kTmemCols = 512;
@@ -43,22 +42,29 @@ constexpr float kRescaleLog2 = 8.f;  // move the running max only past this marg
 
 template <int D>
 struct FCfg {
-    static constexpr int STAGES = D == 128 ? 3 : 4;
-    static constexpr int BOXES = D / 64;               // 64-column boxes per tile row
-    static constexpr uint32_t kTile_B = 128 * D * 2;   // Q, K or V tile
-    static constexpr uint32_t kBox_B = 128 * 128;      // one 64-column box of a tile
+    // key rows per step: 128, or 64 at d = 256 so that Q, two K / V stages and the 256-column O
+    // accumulator fit shared memory and TMEM
+    static constexpr int BN = D <= 128 ? 128 : 64;
+    static constexpr int STAGES = D == 64 ? 4 : (D == 128 ? 3 : 2);
+    static constexpr int NBUF = D <= 128 ? 3 : 2;          // S buffers in TMEM, 128 columns apart
+    static constexpr int BOXES = D / 64;                    // 64-column boxes per tile row
+    static constexpr uint32_t kTileQ_B = BM * D * 2;        // Q tile
+    static constexpr uint32_t kTileKV_B = BN * D * 2;       // K or V tile
+    static constexpr uint32_t kBoxQ_B = BM * 128;           // one 64-column box of the Q tile
+    static constexpr uint32_t kBoxKV_B = BN * 128;          // one 64-column box of a K / V tile
     static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_K = OFF_Q + kTile_B;
-    static constexpr uint32_t OFF_V = OFF_K + STAGES * kTile_B;
-    static constexpr uint32_t OFF_BAR = OFF_V + STAGES * kTile_B;
-    // three S buffers [0,128), [128,256), [256,384); O [384, 384+D)
-    static constexpr uint32_t TM_S = 0, TM_O = 384;
+    static constexpr uint32_t OFF_K = OFF_Q + kTileQ_B;
+    static constexpr uint32_t OFF_V = OFF_K + STAGES * kTileKV_B;
+    static constexpr uint32_t OFF_BAR = OFF_V + STAGES * kTileKV_B;
+    // S buffer b at column 128 b (BN columns used); O after them: [384, 384+D) or [256, 512)
+    static constexpr uint32_t TM_S = 0, TM_O = 128 * NBUF;
+    static_assert(TM_O + D <= 512, "TMEM columns");
 };
 
 enum {
     F_Q = 0,      // Q tile landed (TMA)
-    F_S0,             // S(j) in buffer j % 3 (MMA commit), one slot per buffer
-    F_P0 = F_S0 + 3,  // P(j) packed in buffer j % 3 (4 softmax warps), one slot per buffer
+    F_S0,             // S(j) in buffer j % NBUF (MMA commit), one slot per buffer (up to 3)
+    F_P0 = F_S0 + 3,  // P(j) packed in buffer j % NBUF (4 softmax warps), one slot per buffer
     F_PV0 = F_P0 + 3, // O += P(j) V(j) done (MMA commit), one slot per buffer
     F_FINAL = F_PV0 + 3,  // every product done (P V issuer's last commit)
     F_STAGE0      // then STAGES "full" barriers, then STAGES "empty" barriers
@@ -96,6 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const FParams p, int causal) {
     using C = FCfg<D>;
+    constexpr int BN = C::BN, NB = C::NBUF;
     constexpr bool kBF16 = TypeTraits<T>::kId == FA_BF16;
     constexpr int kNumBars = F_STAGE0 + 2 * C::STAGES;
     constexpr uint32_t OFF_MISC = C::OFF_BAR + kNumBars * 8;
@@ -153,19 +160,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kWarpTma) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && !*abort_flag && n_cnt > 0) {
-            ptx::mbar_arrive_expect_tx(bar(F_Q), C::kTile_B);
+            ptx::mbar_arrive_expect_tx(bar(F_Q), C::kTileQ_B);
             for (int x = 0; x < C::BOXES; ++x)
-                ptx::tma_load_3d(sbase + C::OFF_Q + x * C::kBox_B, &tmQ, x * 64, m0, bh, bar(F_Q));
+                ptx::tma_load_3d(sbase + C::OFF_Q + x * C::kBoxQ_B, &tmQ, x * 64, m0, bh, bar(F_Q));
             int issued = 0;
             for (int j = 0; j < n_cnt; ++j) {
                 const int s = j % C::STAGES;
                 if (j >= C::STAGES && !wait_bar(bar_empty(s), ((j / C::STAGES) - 1) & 1, abort_flag, p.err)) break;
-                ptx::mbar_arrive_expect_tx(bar_full(s), 2 * C::kTile_B);
+                ptx::mbar_arrive_expect_tx(bar_full(s), 2 * C::kTileKV_B);
                 for (int x = 0; x < C::BOXES; ++x) {
-                    ptx::tma_load_3d(sbase + C::OFF_K + s * C::kTile_B + x * C::kBox_B, &tmK, x * 64,
+                    ptx::tma_load_3d(sbase + C::OFF_K + s * C::kTileKV_B + x * C::kBoxKV_B, &tmK, x * 64,
                                      (n_first + j) * BN, bkv,
                                      bar_full(s));
-                    ptx::tma_load_3d(sbase + C::OFF_V + s * C::kTile_B + x * C::kBox_B, &tmV, x * 64,
+                    ptx::tma_load_3d(sbase + C::OFF_V + s * C::kTileKV_B + x * C::kBoxKV_B, &tmV, x * 64,
                                      (n_first + j) * BN, bkv,
                                      bar_full(s));
                 }
@@ -183,10 +190,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // fence it executes leaves the pipe idle.  Two issuers hide each other's bookkeeping:
         // warp 5 issues S = Q K^T, warp 6 issues O += P V.  Products of different threads are
         // not ordered with each other, so every hazard between them goes through a barrier:
-        // S(j) into buffer j % 3 waits until P V(j-3) has read P out of it (one P V barrier per
+        // S(j) into buffer j % NBUF waits until P V(j-NBUF) has read P out of it (one P V barrier per
         // buffer, so that wait can never see a phase two ahead), and P V(j) runs only once the
-        // softmax has turned S(j) into P(j), which implies S(j) is complete.  Three S buffers let
-        // S(j+2) run while the softmax still works on S(j) and S(j+1).
+        // softmax has turned S(j) into P(j), which implies S(j) is complete.  Three S buffers
+        // (d <= 128) let S(j+2) run while the softmax still works on S(j) and S(j+1).
         if (lane == 0 && !*abort_flag && n_cnt > 0) {
             constexpr uint32_t ID_S = ptx::idesc_f16(BM, BN, kBF16, false, false);  // S = Q K^T
             constexpr uint32_t ID_PV = ptx::idesc_f16(BM, D, kBF16, false, true);   // O += P V (A in TMEM)
@@ -199,32 +206,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; ok && j < n_cnt; ++j) {
                     const int s = j % C::STAGES;
                     if (!(ok = wait_bar(bar_full(s), (j / C::STAGES) & 1, abort_flag, p.err))) break;
-                    if (j >= 3 && !(ok = wait_bar(bar(F_PV0 + j % 3), (j / 3 - 1) & 1, abort_flag, p.err))) break;
+                    if (j >= NB && !(ok = wait_bar(bar(F_PV0 + j % NB), (j / NB - 1) & 1, abort_flag, p.err))) break;
                     ptx::tc_fence_after();
-                    const uint32_t so = (uint32_t)s * C::kTile_B;
+                    const uint32_t so = (uint32_t)s * C::kTileKV_B;
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t ko = (k / 4) * C::kBox_B + (k % 4) * 32;
-                        ptx::mma_ss(tmem + C::TM_S + (j % 3) * 128, desc_add(dQ_k, ko), desc_add(dK_k, so + ko), ID_S,
-                                    k > 0);
+                        const uint32_t kq = (k / 4) * C::kBoxQ_B + (k % 4) * 32;
+                        const uint32_t kk = (k / 4) * C::kBoxKV_B + (k % 4) * 32;
+                        ptx::mma_ss(tmem + C::TM_S + (j % NB) * 128, desc_add(dQ_k, kq), desc_add(dK_k, so + kk),
+                                    ID_S, k > 0);
                     }
-                    ptx::mma_commit(bar(F_S0 + j % 3));
+                    ptx::mma_commit(bar(F_S0 + j % NB));
                 }
                 // this thread's products must be complete before TMEM is released; every S it
                 // issued is read by a P V product, so they are, once the P V issuer drained
             } else {
-                const uint64_t dV_mn = ptx::sw128_desc(sbase + C::OFF_V, C::kBox_B, 1024);  // + stage offset
+                const uint64_t dV_mn = ptx::sw128_desc(sbase + C::OFF_V, C::kBoxKV_B, 1024);  // + stage offset
                 for (int j = 0; ok && j < n_cnt; ++j) {
                     const int s = j % C::STAGES;
-                    // O += P(j) V(j)   (A = P packed in buffer j % 3: 16 keys = 8 packed columns per step)
-                    if (!(ok = wait_bar(bar(F_P0 + j % 3), (j / 3) & 1, abort_flag, p.err))) break;
+                    // O += P(j) V(j)   (A = P packed in buffer j % NBUF: 16 keys = 8 packed columns per step)
+                    if (!(ok = wait_bar(bar(F_P0 + j % NB), (j / NB) & 1, abort_flag, p.err))) break;
                     ptx::tc_fence_after();
 #pragma unroll
                     for (int k = 0; k < BN / 16; ++k)
-                        ptx::mma_ts(tmem + C::TM_O, tmem + C::TM_S + (j % 3) * 128 + k * 8,
-                                    desc_add(dV_mn, (uint32_t)s * C::kTile_B + k * 2048), ID_PV,
+                        ptx::mma_ts(tmem + C::TM_O, tmem + C::TM_S + (j % NB) * 128 + k * 8,
+                                    desc_add(dV_mn, (uint32_t)s * C::kTileKV_B + k * 2048), ID_PV,
                                     (j > 0 || k > 0) ? 1u : 0u);
-                    ptx::mma_commit(bar(F_PV0 + j % 3));
+                    ptx::mma_commit(bar(F_PV0 + j % NB));
                     ptx::mma_commit(bar_empty(s));  // K(j), V(j) no longer read (S(j) completed before P(j))
                 }
                 // no MMA may still write TMEM when it is released
@@ -243,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float l_run = 0.f;        // sum of exp2(x - m_run)
         bool ok = !*abort_flag;
         for (int j = 0; ok && j < n_cnt; ++j) {
-            const uint32_t buf = tmem + C::TM_S + (j % 3) * 128 + lane_off;
+            const uint32_t buf = tmem + C::TM_S + (j % NB) * 128 + lane_off;
             const int n0 = (n_first + j) * BN;
             // Key columns c of this tile (key n0 + c) that the row sees form one interval
             // (visible_keys of the row's key position i + off), cut to the keys that exist.
@@ -254,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const unsigned c_span = c_hi > c_lo ? (unsigned)(c_hi - c_lo) : 0u;
             // warp-uniform: the chosen path holds .sync.aligned TMEM accesses
             const bool masked = __any_sync(0xffffffffu, !(c_lo <= 0 && c_hi >= BN));
-            if (!(ok = wait_bar_warp(bar(F_S0 + j % 3), (j / 3) & 1, abort_flag, p.err))) break;
+            if (!(ok = wait_bar_warp(bar(F_S0 + j % NB), (j / NB) & 1, abort_flag, p.err))) break;
             ptx::tc_fence_after();
             uint32_t r[BN];
 #pragma unroll
@@ -301,11 +309,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 s2 = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
             const float sum = s2.x + s2.y;
             l_run = l_run * alpha + sum;
-            ptx::tmem_st32(buf, Pp);  // packed P into columns [0, 64): already read
-            ptx::tmem_st32(buf + 32, Pp + 32);
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c)  // packed P into columns [0, BN/2): already read
+                ptx::tmem_st32(buf + c * 32, Pp + c * 32);
             // rescale the O row before the next P V product accumulates into it
             if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-                if (!(ok = wait_bar_warp(bar(F_PV0 + (j - 1) % 3), ((j - 1) / 3) & 1, abort_flag, p.err))) break;
+                if (!(ok = wait_bar_warp(bar(F_PV0 + (j - 1) % NB), ((j - 1) / NB) & 1, abort_flag, p.err))) break;
                 ptx::tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -320,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(F_P0 + j % 3));
+            if (lane == 0) ptx::mbar_arrive(bar(F_P0 + j % NB));
         }
         // ---- epilogue: O = acc / l, LSE = (m + log2 l) * ln 2.  Wait for the MMA issuer's
         // final commit (every product done), not for a parity of the shared P V barrier:
@@ -384,14 +393,15 @@ EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-// 3-D view [heads][rows][D] of a [B, heads, rows, D] 16-bit tensor: 64-column x 128-row
-// boxes with 128-byte swizzle (rows past the end read as zeros).
-bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int heads, int rows, int D) {
+// 3-D view [heads][rows][D] of a [B, heads, rows, D] 16-bit tensor: 64-column x box_rows-row
+// boxes with 128-byte swizzle (rows and columns past the end read as zeros).
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int heads, int rows, int D,
+              int box_rows) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)heads};
     const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)rows * D * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -408,8 +418,9 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, void* O, float
         TypeTraits<T>::kId == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap tq, tk, tv;
     // global extents and strides use the tensors' head dim s.d; the kernel reads D columns
-    if (s.d > D || s.d % 32 != 0 || !make_map(&tq, Q, dt, s.B * s.H, s.S_q, s.d) ||
-        !make_map(&tk, K, dt, s.B * s.H_kv, s.S_k, s.d) || !make_map(&tv, V, dt, s.B * s.H_kv, s.S_k, s.d))
+    if (s.d > D || s.d % 32 != 0 || !make_map(&tq, Q, dt, s.B * s.H, s.S_q, s.d, BM) ||
+        !make_map(&tk, K, dt, s.B * s.H_kv, s.S_k, s.d, C::BN) ||
+        !make_map(&tv, V, dt, s.B * s.H_kv, s.S_k, s.d, C::BN))
         return cudaErrorInvalidValue;
     FParams p;
     p.O = O;
@@ -435,8 +446,12 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, void* O, float
 
 cudaError_t launch_fwd_sm103(int dtype, const void* Q, const void* K, const void* V, void* O, float* LSE,
                             unsigned int* err, const Shape& s, cudaStream_t st) {
-    const int D = tc_head_dim(s.d);  // d = 32 / 96 run the 64 / 128 kernels
-    if (D == 64) {
+    // every head dim the library takes: d = 32 / 96 run the 64 / 128 kernels, d = 256 its own
+    const int D = s.d == 256 ? 256 : tc_head_dim(s.d);
+    if (D == 256) {
+        if (dtype == FA_F16) return launch_t<__half, 256>(Q, K, V, O, LSE, err, s, st);
+        if (dtype == FA_BF16) return launch_t<__nv_bfloat16, 256>(Q, K, V, O, LSE, err, s, st);
+    } else if (D == 64) {
         if (dtype == FA_F16) return launch_t<__half, 64>(Q, K, V, O, LSE, err, s, st);
         if (dtype == FA_BF16) return launch_t<__nv_bfloat16, 64>(Q, K, V, O, LSE, err, s, st);
     } else if (D == 128) {

@@ -105,9 +105,9 @@ int fa_bwd_preprocess(const void* dO, const void* O, float* D, int B, int H, int
  * LSE_i = log sum_j exp(scale <Q_i, K_j>) over the visible keys.
  *   Q : [B, H, S_q, d], K, V : [B, H_kv, S_k, d], O : [B, H, S_q, d] dtype;
  *   LSE : [B, H, S_q] float32.  Rows that see no key get O = 0, LSE = -inf.
- * F16/BF16 with d <= 128 run a tcgen05 tensor-core kernel (fp32
- * accumulation, online softmax over 128-key tiles); F32 and d = 256 run an
- * FFMA kernel.
+ * F16/BF16 run a tcgen05 tensor-core kernel (fp32 accumulation, online
+ * softmax over 128-key tiles, 64-key tiles at d = 256); F32 runs an FFMA
+ * kernel.
  */
 int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
            int H_kv, int S_q, int S_k, int d, float scale, int causal, int dtype, void* stream);

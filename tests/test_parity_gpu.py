@@ -176,7 +176,9 @@ def test_preprocess_entry_point(dt, d, S):
     # tensor-core forward: one tile, several tiles with the diagonal, keys past the queries,
     # rows that see no key (S_q > S_k, causal), a single element
     ("bf16", False, 128, 128, 128), ("bf16", True, 1000, 1000, 128), ("f16", True, 130, 1030, 128),
-    ("bf16", True, 260, 130, 128), ("bf16", False, 200, 700, 64), ("f16", False, 1, 1, 64)])
+    ("bf16", True, 260, 130, 128), ("bf16", False, 200, 700, 64), ("f16", False, 1, 1, 64),
+    # d = 256: 64-key tiles, two S buffers (ragged tails of both kinds, rows with no key)
+    ("bf16", True, 300, 300, 256), ("f16", False, 129, 1000, 256), ("bf16", True, 200, 70, 256)])
 def test_forward_helper(dt, causal, S_q, S_k, d):
     w = Workload("fwd", dt, 1, 4, 2, S_q, S_k, d, causal, seed=8)
     Q, K, V, _ = make_inputs(w)
@@ -341,8 +343,9 @@ HEAD_DIMS = [
     ("bf16", 1, 4, 1, 260, 260, 32, True, 0, False),    # tensor cores, 64-wide kernel
     ("f16", 2, 2, 2, 130, 390, 32, False, 100, False),  # + window
     ("bf16", 1, 4, 2, 333, 333, 96, True, 0, True),     # + deterministic dQ
-    ("bf16", 1, 2, 1, 200, 200, 256, True, 0, False),   # d = 256: CUDA-core kernels
+    ("bf16", 1, 2, 1, 200, 200, 256, True, 0, False),   # d = 256: tensor-core forward, CUDA-core backward
     ("f16", 1, 2, 2, 130, 70, 256, False, 0, True),
+    ("bf16", 2, 2, 1, 500, 500, 256, True, 130, False),  # + window
     ("f32", 1, 2, 1, 150, 150, 96, True, 0, False),
     ("f32", 1, 2, 2, 100, 160, 32, False, 30, True),
     ("f32", 1, 2, 1, 90, 90, 256, True, 0, False),
