@@ -67,6 +67,11 @@ constexpr uint32_t kDrainBarrier = 1;                           // named barrier
 template <int D>
 struct Cfg {
     static constexpr int STAGES = D == 128 ? 2 : 3;
+    // d = 64 leaves TMEM room for a third S / dP buffer (dV, dK take 64 columns each) and
+    // shared memory for a second dS tile, so S(i+1) need not wait for the dK product of
+    // iteration i, nor dS(i+1) for the dQ(i) reduce to read the dS tile
+    static constexpr int NBUF = D == 64 ? 3 : 2;  // 128-column TMEM buffers
+    static constexpr int NDS = D == 64 ? 2 : 1;   // shared dS tiles
     static constexpr int BOXES = D / 64;                 // 64-column boxes per tile row
     static constexpr uint32_t kTileK_B = BN * D * 2;     // K or V tile bytes
     static constexpr uint32_t kTileQ_B = BM * D * 2;     // Q or dO tile bytes
@@ -78,28 +83,29 @@ struct Cfg {
     static constexpr uint32_t OFF_Q = OFF_V + kTileK_B;
     static constexpr uint32_t OFF_DO = OFF_Q + STAGES * kTileQ_B;
     static constexpr uint32_t OFF_DS = OFF_DO + STAGES * kTileQ_B;
-    static constexpr uint32_t OFF_LSE = OFF_DS + kdS_B;
+    static constexpr uint32_t OFF_LSE = OFF_DS + NDS * kdS_B;
     static constexpr uint32_t OFF_DD = OFF_LSE + STAGES * BM * 4;
     static constexpr uint32_t OFF_BAR = OFF_DD + STAGES * BM * 4;
-    static constexpr uint32_t kNumBars = 13 + 2 * STAGES;  // B_STAGE0 + 2 * STAGES
+    static constexpr uint32_t kNumBars = 19 + 2 * STAGES;  // B_STAGE0 + 2 * STAGES
     static constexpr uint32_t OFF_MISC = OFF_BAR + kNumBars * 8;
     static constexpr uint32_t SMEM = OFF_MISC + 16;
     static constexpr uint32_t TM_DV = 0, TM_DK = D, TM_BUF0 = 2 * D;
+    static_assert(TM_BUF0 + 128 * NBUF <= kTmemCols, "TMEM columns");
     static_assert(kdS_B == 2 * BM * 128, "the dS tile doubles as two 128-row x 32-fp32 dQ staging boxes");
 };
 
 // Barrier slots.
 enum {
     B_KV = 0,      // K, V landed (TMA)
-    B_S_FULL,      // S(i) in TMEM (MMA commit)
-    B_DP_FULL,     // dP(i) in TMEM (MMA commit)
-    B_P_READY,     // P(i) packed in TMEM (8 softmax warps)
-    B_DS_READY,    // dS(i) packed in TMEM and in shared memory (8 softmax warps)
-    B_DS_EMPTY,    // shared dS tile free again: dQ(i) staged out of it and read by TMA (drain)
-    B_DQ_FULL,     // dQ(i) in TMEM (MMA commit)
+    B_S_FULL,      // S(i) in TMEM (MMA commit); one per TMEM buffer when there are 3
+    B_DP_FULL = B_S_FULL + 3,  // dP(i) in TMEM (MMA commit)
+    B_P_READY,     // P(i) packed in TMEM (8 softmax warps); one per TMEM buffer when there are 3
+    B_DS_READY = B_P_READY + 3,  // dS(i) packed in TMEM and in shared memory (8 softmax warps)
+    B_DS_EMPTY,    // a shared dS tile free again: dQ(i) staged out of it and read by TMA; one per tile
+    B_DQ_FULL = B_DS_EMPTY + 2,  // dQ(i) in TMEM (MMA commit)
     B_DQ_EMPTY,    // dQ(i) copied out of TMEM (4 drain warps)
-    B_DQ_STAGED,   // dQ(i) staged in shared memory for the bulk reduce (4 drain warps)
-    B_G3,          // dV product of iteration i done (MMA commit)
+    B_DQ_STAGED,   // dQ(i) staged in dS tile dt(i) for the deterministic adds (4 drain warps); one per tile
+    B_G3 = B_DQ_STAGED + 2,          // dV product of iteration i done (MMA commit)
     B_G4,          // dK product of iteration i done (MMA commit)
     B_ACC,         // every product done: dK / dV final (MMA commit)
     B_FINAL,       // MMA shutdown
@@ -143,7 +149,7 @@ __device__ __forceinline__ float2 unpack2(uint32_t v) {
     return __half22float2(*reinterpret_cast<__half2*>(&v));
 }
 
-static_assert(B_STAGE0 == 13, "Cfg::kNumBars counts 13 named barriers before the stage ring");
+static_assert(B_STAGE0 == 19, "Cfg::kNumBars counts 19 named barriers before the stage ring");
 
 template <typename T, int D, bool kDet>
 __global__ void __launch_bounds__(threads_for(kDet), 1)
@@ -198,8 +204,8 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
         if ((sbase & 1023u) != 0) atomicOr(p.err, kErrSmemAlign);
         *abort_flag = (sbase & 1023u) != 0;
         for (int i = 0; i < (int)C::kNumBars; ++i) {
-            uint32_t count = (i == B_P_READY || i == B_DS_READY) ? (uint32_t)kNumSoftWarps
-                             : i == B_DQ_EMPTY || i == B_DQ_STAGED ? 4u
+            uint32_t count = ((i >= B_P_READY && i < B_P_READY + 3) || i == B_DS_READY) ? (uint32_t)kNumSoftWarps
+                             : (i == B_DQ_EMPTY || i == B_DQ_STAGED || i == B_DQ_STAGED + 1) ? 4u
                                                                : 1u;
             if (D == 128 && i >= B_STAGE0 + C::STAGES) count = 2;  // stage "empty": MMA + drain
             ptx::mbar_init(bar(i), count);
@@ -217,6 +223,21 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
     const uint32_t tmem = *tmem_slot;
     const uint32_t tm_buf0 = tmem + C::TM_BUF0;  // buffer x at tm_buf0 + 128 * x
 
+    // Buffer roles.  Iteration i computes S(i) -> P(i) -> dQ(i) in buffer xb(i) and
+    // dP(i) -> dS(i) in buffer yb(i); dP(i+1) always goes into xb(i) once dQ(i) left it.
+    // Two buffers: S(i+1) goes into yb(i) once the dK product of iteration i has read dS(i).
+    // Three: buffer k serves as xb(i), yb(i+1), xb(i+3), ..., so S(i+1) goes into yb(i-1),
+    // free once the dK product of iteration i-1 is done, and runs while the softmax still
+    // works on iteration i.  Each buffer then has its own S / P barriers (its uses are three
+    // iterations apart, so no parity wait can see a phase two ahead).  dS(i) is staged in
+    // shared dS tile dt(i).
+    constexpr int NBUF = C::NBUF, NDS = C::NDS;
+    auto xb = [](int i) { return NBUF == 3 ? (2 * i) % 3 : (i & 1); };
+    auto yb = [](int i) { return NBUF == 3 ? (2 * i + 1) % 3 : ((i & 1) ^ 1); };
+    auto sp_slot = [](int i) { return NBUF == 3 ? (2 * i) % 3 : 0; };  // S / P barrier of iteration i
+    auto sp_par = [](int i) { return NBUF == 3 ? (i / 3) & 1 : i & 1; };
+    auto dt = [](int i) { return NDS == 2 ? (i & 1) : 0; };
+
     auto iter_coords = [&](int it, int& bh, int& m0) {
         const int hh = it % g;
         m0 = (m_end - 1 - it / g) * BM;
@@ -226,10 +247,11 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
     // releases once TMA has read each staging area: the dS tile (B_DS_EMPTY) and, at
     // d = 128, the Q / dO stage, whose second arrival (after the MMA warp's, once the dK
     // product that reads Q is done) lets the next load in.
-    auto reduce_staged = [&](int s, int bh, int m0, bool add) {
+    auto reduce_staged = [&](int s, int tile, int bh, int m0, bool add) {
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {  // one bulk group per staging area, dS tile first
-            const uint32_t area = sbase + (h == 0 ? C::OFF_DS : C::OFF_DO + s * C::kTileQ_B);
+            const uint32_t area =
+                sbase + (h == 0 ? C::OFF_DS + tile * C::kdS_B : C::OFF_DO + s * C::kTileQ_B);
             if (add) {  // 32-column boxes past the head dim hold zeros and are not added
                 // the accumulator lines stay in L2 ahead of the Q / dO stream: the
                 // finalise pass then reads much of dQacc from L2
@@ -241,12 +263,12 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
         }
         if (D == 128) {
             ptx::bulk_wait_read_1();  // the dS-tile group (the older one) was read
-            ptx::mbar_arrive(bar(B_DS_EMPTY));
+            ptx::mbar_arrive(bar(B_DS_EMPTY + tile));
             ptx::bulk_wait_read_all();
             ptx::mbar_arrive(bar_empty(s));  // second of two arrivals (MMA commit after dK)
         } else {
             ptx::bulk_wait_read_all();
-            ptx::mbar_arrive(bar(B_DS_EMPTY));
+            ptx::mbar_arrive(bar(B_DS_EMPTY + tile));
         }
     };
     constexpr bool det = kDet;  // p.dq_sem holds the turn counters
@@ -290,7 +312,7 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
             constexpr uint32_t ID_SD = ptx::idesc_f16(BN, BM, kBF16, false, false);  // S^T, dP^T
             constexpr uint32_t ID_KV = ptx::idesc_f16(BN, D, kBF16, false, true);    // dV, dK (A in TMEM)
             constexpr uint32_t ID_Q = ptx::idesc_f16(BM, D, kBF16, true, true);      // dQ
-            const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sdS = sbase + C::OFF_DS;
+            const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
             // S^T = K Q^T or dP^T = V dO^T into a TMEM buffer; both operands K-major.
             auto gemm_sd = [&](uint32_t d_tmem, uint32_t a_base, uint32_t b_base) {
 #pragma unroll
@@ -305,20 +327,31 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
             if (ok) ok = wait_bar(bar_full(0), 0, abort_flag, p.err);
             if (ok) {
                 ptx::tc_fence_after();
-                gemm_sd(tm_buf0, sK, sbase + C::OFF_Q);
-                ptx::mma_commit(bar(B_S_FULL));
-                gemm_sd(tm_buf0 + 128, sV, sbase + C::OFF_DO);
+                gemm_sd(tm_buf0 + 128 * xb(0), sK, sbase + C::OFF_Q);
+                ptx::mma_commit(bar(B_S_FULL + sp_slot(0)));
+                gemm_sd(tm_buf0 + 128 * yb(0), sV, sbase + C::OFF_DO);
                 ptx::mma_commit(bar(B_DP_FULL));
             }
             for (int it = 0; ok && it < n_it; ++it) {
                 const int s = it % C::STAGES;
-                const uint32_t X = tm_buf0 + 128 * (it & 1);        // S -> P -> dQ of this iteration
-                const uint32_t Y = tm_buf0 + 128 * ((it & 1) ^ 1);  // dP -> dS of this iteration, S of the next
+                const int s1 = (it + 1) % C::STAGES;
+                const uint32_t X = tm_buf0 + 128 * xb(it);  // S -> P -> dQ of this iteration
+                const uint32_t Y = tm_buf0 + 128 * yb(it);  // dP -> dS of this iteration
                 const uint32_t sQ = sbase + C::OFF_Q + s * C::kTileQ_B;
                 const uint32_t sdO = sbase + C::OFF_DO + s * C::kTileQ_B;
+                const uint32_t sdS = sbase + C::OFF_DS + dt(it) * C::kdS_B;
+                if (NBUF == 3 && it + 1 < n_it) {
+                    // S(i+1) into yb(i-1) once Q(i+1) is in and the dK product of iteration
+                    // i-1 stopped reading dS(i-1) from it (the first iteration's is unused)
+                    if (!(ok = wait_bar(bar_full(s1), ((it + 1) / C::STAGES) & 1, abort_flag, p.err))) break;
+                    if (it > 0 && !(ok = wait_bar(bar(B_G4), (it - 1) & 1, abort_flag, p.err))) break;
+                    ptx::tc_fence_after();
+                    gemm_sd(tm_buf0 + 128 * xb(it + 1), sK, sbase + C::OFF_Q + s1 * C::kTileQ_B);
+                    ptx::mma_commit(bar(B_S_FULL + sp_slot(it + 1)));
+                }
                 // dV += P^T dO.  A = P^T in TMEM: queries [0,64) packed in X[0,32), queries
                 // [64,128) in X[64,96); 16 queries = 8 packed columns per step.
-                if (!(ok = wait_bar(bar(B_P_READY), it & 1, abort_flag, p.err))) break;
+                if (!(ok = wait_bar(bar(B_P_READY + sp_slot(it)), sp_par(it), abort_flag, p.err))) break;
                 ptx::tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < BM / 16; ++k)
@@ -345,13 +378,14 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
                 // the drain also arrived: it stages half of dQ(i) in the dO tile)
                 ptx::mma_commit(bar_empty(s));
                 if (it + 1 < n_it) {
-                    // S(i+1) into Y once the dK product stopped reading dS(i) from it
-                    const int s1 = (it + 1) % C::STAGES;
-                    if (!(ok = wait_bar(bar_full(s1), ((it + 1) / C::STAGES) & 1, abort_flag, p.err))) break;
-                    if (!(ok = wait_bar(bar(B_G4), it & 1, abort_flag, p.err))) break;
-                    ptx::tc_fence_after();
-                    gemm_sd(Y, sK, sbase + C::OFF_Q + s1 * C::kTileQ_B);
-                    ptx::mma_commit(bar(B_S_FULL));
+                    if (NBUF == 2) {
+                        // S(i+1) into Y once the dK product stopped reading dS(i) from it
+                        if (!(ok = wait_bar(bar_full(s1), ((it + 1) / C::STAGES) & 1, abort_flag, p.err))) break;
+                        if (!(ok = wait_bar(bar(B_G4), it & 1, abort_flag, p.err))) break;
+                        ptx::tc_fence_after();
+                        gemm_sd(Y, sK, sbase + C::OFF_Q + s1 * C::kTileQ_B);
+                        ptx::mma_commit(bar(B_S_FULL + sp_slot(it + 1)));
+                    }
                     // dP(i+1) into X once dQ(i) left it
                     if (!(ok = wait_bar(bar(B_DQ_EMPTY), it & 1, abort_flag, p.err))) break;
                     ptx::tc_fence_after();
@@ -383,8 +417,8 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
         bool ok = !*abort_flag;
         for (int it = 0; ok && it < n_it; ++it) {
             const int s = it % C::STAGES;
-            const uint32_t X = tm_buf0 + 128 * (it & 1) + lane_off + qh;
-            const uint32_t Y = tm_buf0 + 128 * ((it & 1) ^ 1) + lane_off + qh;
+            const uint32_t X = tm_buf0 + 128 * xb(it) + lane_off + qh;
+            const uint32_t Y = tm_buf0 + 128 * yb(it) + lane_off + qh;
             int bh, m0;
             iter_coords(it, bh, m0);
             const int i_lo = m0 + qh;  // first query row of this warp's columns
@@ -404,7 +438,7 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
             const float* sl = reinterpret_cast<const float*>(smem + C::OFF_LSE + s * BM * 4) + qh;
             const float* sd = reinterpret_cast<const float*>(smem + C::OFF_DD + s * BM * 4) + qh;
             if (!(ok = wait_bar_warp(bar_full(s), (it / C::STAGES) & 1, abort_flag, p.err))) break;
-            if (!(ok = wait_bar_warp(bar(B_S_FULL), it & 1, abort_flag, p.err))) break;
+            if (!(ok = wait_bar_warp(bar(B_S_FULL + sp_slot(it)), sp_par(it), abort_flag, p.err))) break;
             ptx::tc_fence_after();
             // P = exp2(S * scale*log2e - LSE*log2e), packed to 16 bits in place.  Masking is
             // decided once per warp, outside the unrolled loop, so the 64 independent exp
@@ -446,12 +480,15 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(B_P_READY));
+            if (lane == 0) ptx::mbar_arrive(bar(B_P_READY + sp_slot(it)));
 
             // dS = P * (dP - D): packed in place into this warp's first 32 columns of Y for
             // the dK product, and into the shared dS tile for dQ.
             if (!(ok = wait_bar_warp(bar(B_DP_FULL), it & 1, abort_flag, p.err))) break;
-            if (it > 0 && !(ok = wait_bar_warp(bar(B_DS_EMPTY), (it - 1) & 1, abort_flag, p.err))) break;
+            // the dS tile of this iteration was last used NDS iterations ago
+            if (it >= NDS &&
+                !(ok = wait_bar_warp(bar(B_DS_EMPTY + dt(it)), ((it - NDS) / NDS) & 1, abort_flag, p.err)))
+                break;
             ptx::tc_fence_after();
             {
                 uint32_t r[kHalfQ];
@@ -477,7 +514,7 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
                 ptx::tmem_st32(Y, pk);  // columns already read
 #pragma unroll
                 for (int u = 0; u < kHalfQ / 8; ++u)  // 8 queries = one 16-byte chunk
-                    *reinterpret_cast<uint4*>(sdS_row + ((u ^ (t & 7)) << 4)) =
+                    *reinterpret_cast<uint4*>(sdS_row + dt(it) * C::kdS_B + ((u ^ (t & 7)) << 4)) =
                         make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
             }
             ptx::tmem_wait_st();
@@ -539,7 +576,7 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
         bool ok = !*abort_flag;
         for (int it = 0; ok && it < n_it; ++it) {
             const int s = it % C::STAGES;
-            const uint32_t X = tm_buf0 + 128 * (it & 1) + lane_off;
+            const uint32_t X = tm_buf0 + 128 * xb(it) + lane_off;
             int bh, m0;
             iter_coords(it, bh, m0);
             // all four drain warps take the same decision (each arrives on B_DQ_STAGED below)
@@ -562,7 +599,7 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(bar(B_DQ_EMPTY));
                 }
-                uint8_t* area = smem + (h == 0 ? C::OFF_DS : C::OFF_DO + s * C::kTileQ_B);
+                uint8_t* area = smem + (h == 0 ? C::OFF_DS + dt(it) * C::kdS_B : C::OFF_DO + s * C::kTileQ_B);
 #pragma unroll
                 for (int bx = 0; bx < 2; ++bx)
 #pragma unroll
@@ -575,10 +612,10 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
             ptx::fence_proxy_async_smem();  // the staged dQ before the bulk reads
             if (det) {  // the reduce warp takes the turn and issues the adds
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(B_DQ_STAGED));
+                if (lane == 0) ptx::mbar_arrive(bar(B_DQ_STAGED + dt(it)));
             } else {
                 ptx::named_bar_sync(kDrainBarrier, 128);
-                if (t == 0) reduce_staged(s, bh, m0, true);
+                if (t == 0) reduce_staged(s, dt(it), bh, m0, true);
             }
         }
         if (!det && t == 0) ptx::bulk_wait_all();
@@ -596,7 +633,9 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
                 const int s = it % C::STAGES;
                 int bh, m0;
                 iter_coords(it, bh, m0);
-                if (!(ok = wait_bar(bar(B_DQ_STAGED), it & 1, abort_flag, p.err))) break;
+                // one barrier per dS tile: with two tiles the drain may stage dQ(i+1) before
+                // this thread waits for dQ(i), so a shared barrier could run two phases ahead
+                if (!(ok = wait_bar(bar(B_DQ_STAGED + dt(it)), (it / NDS) & 1, abort_flag, p.err))) break;
                 // Deterministic dQ: the key tiles that touch this query tile add into it in
                 // key-tile order.  Turn t of the tile's counter belongs to its t-th such key
                 // tile (they are consecutive: the first is where key_range of the query tile
@@ -610,7 +649,7 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
                 unsigned int* sem = p.dq_sem + (size_t)bh * m_tiles + m0 / BM;
                 const bool go = wait_counter(sem, turn, abort_flag, p.err);
                 ptx::fence_proxy_async_global();  // the earlier turns' adds before ours
-                reduce_staged(s, bh, m0, go);
+                reduce_staged(s, dt(it), bh, m0, go);
                 if (prev_sem != nullptr) {
                     // the previous tile's groups are complete once at most this tile's are pending
                     ptx::bulk_wait_pending<D / 64>();
