@@ -126,6 +126,9 @@ EDGE = [
     ("f32", 1, 4, 2, 200, 200, 128, True),
     ("f32", 2, 2, 1, 65, 33, 64, False),
     ("f32", 1, 2, 2, 33, 65, 64, True),
+    # non-causal with 8 (batch, kv head) groups: the CTAs run in two blocks of 4 groups
+    ("bf16", 2, 8, 4, 300, 300, 128, False),
+    ("f16", 4, 4, 2, 200, 333, 64, False),
 ]
 
 
@@ -248,6 +251,7 @@ WINDOW = [
     ("f16", 1, 2, 1, 333, 333, 64, True, 1),        # diagonal only
     ("bf16", 1, 2, 2, 256, 256, 128, True, 128),    # band edge on tile boundaries
     ("bf16", 2, 4, 1, 1024, 1024, 64, True, 4096),  # wider than the problem: plain causal
+    ("bf16", 2, 8, 4, 400, 400, 64, True, 100),     # 8 groups: two blocks of 4 in the CTA order
     ("f32", 1, 2, 1, 200, 200, 64, True, 37),
     ("f32", 1, 2, 2, 150, 90, 128, False, 20),
 ]
@@ -292,6 +296,8 @@ DET = [
     ("f16", 1, 4, 4, 513, 300, 64, False, 0),       # S_q > S_k, d = 64
     ("bf16", 1, 4, 1, 300, 600, 128, True, 200),    # window: turns start past key tile 0
     ("bf16", 1, 2, 2, 600, 600, 64, False, 130),    # two-sided window
+    ("bf16", 2, 8, 2, 300, 700, 64, False, 0),      # d = 64 GQA: 12 iterations per CTA, both dS tiles
+    ("f16", 2, 8, 4, 300, 300, 128, False, 0),      # 8 groups, non-causal: order stays interleaved
     ("f32", 1, 4, 2, 200, 333, 128, True, 0),       # CUDA-core dQ kernel
     ("f32", 1, 2, 1, 150, 150, 64, False, 40),
 ]
