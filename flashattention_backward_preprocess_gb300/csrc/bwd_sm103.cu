@@ -53,13 +53,15 @@ namespace {
 constexpr int BM = kTileQ;  // 128 query rows per iteration
 constexpr int BN = kTileK;  // 128 key rows per CTA
 static_assert(BM == 128, "the packed P / dS column layout assumes two 64-query halves");
-// 14 warps; deterministic mode adds a 15th (kWarpRed)
-constexpr int threads_for(bool det) { return det ? 480 : 448; }
+// 14 warps; d = 64 adds a second MMA-issuing warp (kWarpMma2) and deterministic mode a warp for
+// the dQ turns (red_warp)
+__host__ __device__ constexpr int threads_for(bool det, int D) { return 32 * (14 + (D == 64) + det); }
+__host__ __device__ constexpr int red_warp(int D) { return D == 64 ? 15 : 14; }
 // warps 0-3 drain dQ; warps 4-11 compute P / dS (two warps per TMEM lane quadrant, one
 // per half of the query columns); warp 12 issues TMA; warp 13 owns TMEM and issues MMAs;
 // warp 14, in deterministic mode, takes the dQ turns and issues the dQ reduce-adds
 constexpr int kWarpDrain0 = 0, kWarpSoft0 = 4, kNumSoftWarps = 8, kWarpTma = 12, kWarpMma = 13,
-              kWarpRed = 14;
+              kWarpMma2 = 14;
 constexpr int kHalfQ = BM / 2;  // query columns per softmax warp
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDrainBarrier = 1;                           // named barrier of the drain warps
@@ -86,7 +88,7 @@ struct Cfg {
     static constexpr uint32_t OFF_LSE = OFF_DS + NDS * kdS_B;
     static constexpr uint32_t OFF_DD = OFF_LSE + STAGES * BM * 4;
     static constexpr uint32_t OFF_BAR = OFF_DD + STAGES * BM * 4;
-    static constexpr uint32_t kNumBars = 19 + 2 * STAGES;  // B_STAGE0 + 2 * STAGES
+    static constexpr uint32_t kNumBars = 23 + 2 * STAGES;  // B_STAGE0 + 2 * STAGES
     static constexpr uint32_t OFF_MISC = OFF_BAR + kNumBars * 8;
     static constexpr uint32_t SMEM = OFF_MISC + 16;
     static constexpr uint32_t TM_DV = 0, TM_DK = D, TM_BUF0 = 2 * D;
@@ -109,7 +111,9 @@ enum {
     B_G4,          // dK product of iteration i done (MMA commit)
     B_ACC,         // every product done: dK / dV final (MMA commit)
     B_FINAL,       // MMA shutdown
-    B_STAGE0       // then STAGES "full" barriers, then STAGES "empty" barriers
+    B_FINAL_A,     // S / dP issuer shutdown (two issuers)
+    B_YFREE,       // two issuers: the dK product of the iteration that used buffer k as Y is done
+    B_STAGE0 = B_YFREE + 3  // then STAGES "full" barriers, then STAGES "empty" barriers
 };
 
 struct Params {
@@ -149,10 +153,10 @@ __device__ __forceinline__ float2 unpack2(uint32_t v) {
     return __half22float2(*reinterpret_cast<__half2*>(&v));
 }
 
-static_assert(B_STAGE0 == 19, "Cfg::kNumBars counts 19 named barriers before the stage ring");
+static_assert(B_STAGE0 == 23, "Cfg::kNumBars counts 23 named barriers before the stage ring");
 
 template <typename T, int D, bool kDet>
-__global__ void __launch_bounds__(threads_for(kDet), 1)
+__global__ void __launch_bounds__(threads_for(kDet, D), 1)
     bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                      const __grid_constant__ CUtensorMap tmdQ, const Params p) {
@@ -306,8 +310,19 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
             for (int it = issued - C::STAGES < 0 ? 0 : issued - C::STAGES; it < issued; ++it)
                 drain_wait(bar_full(it % C::STAGES), (it / C::STAGES) & 1);
         }
-    } else if (warp == kWarpMma) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == kWarpMma || (NBUF == 3 && warp == kWarpMma2)) {
+        // ------------------------------------------------------------ MMA issuers
+        // With two TMEM buffers warp 13 issues every product.  With three (d = 64) warp 13
+        // issues S and dP and warp 14 dV, dQ and dK, so that no product waits behind another's
+        // inputs in one thread's program order (measured with clock64 stamps: one issuer
+        // waiting for the dK product of iteration i-1 before S(i+1) saw P(i) ~2.4K cycles
+        // late).  Every hazard between the two is on a barrier: S(i+1) into yb(i-1) waits for
+        // that buffer's Y-free barrier (the dK product of iteration i-1, one barrier per
+        // buffer, so no wait can see a phase two ahead), dP(i+1) into xb(i) for the drain's
+        // B_DQ_EMPTY; the dV, dQ and dK products follow the softmax's P and dS barriers, which
+        // imply S(i) and dP(i) are complete.
+        const bool issue_sd = NBUF == 2 || warp == kWarpMma;  // S and dP products
+        const bool issue_g = NBUF == 2 || warp == kWarpMma2;  // dV, dQ and dK products
         if (lane == 0 && !*abort_flag && n_it > 0) {
             constexpr uint32_t ID_SD = ptx::idesc_f16(BN, BM, kBF16, false, false);  // S^T, dP^T
             constexpr uint32_t ID_KV = ptx::idesc_f16(BN, D, kBF16, false, true);    // dV, dK (A in TMEM)
@@ -323,14 +338,17 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
                                 ptx::sw128_desc(b_base + koffb, 16, 1024), ID_SD, k > 0);
                 }
             };
-            bool ok = wait_bar(bar(B_KV), 0, abort_flag, p.err);
-            if (ok) ok = wait_bar(bar_full(0), 0, abort_flag, p.err);
-            if (ok) {
-                ptx::tc_fence_after();
-                gemm_sd(tm_buf0 + 128 * xb(0), sK, sbase + C::OFF_Q);
-                ptx::mma_commit(bar(B_S_FULL + sp_slot(0)));
-                gemm_sd(tm_buf0 + 128 * yb(0), sV, sbase + C::OFF_DO);
-                ptx::mma_commit(bar(B_DP_FULL));
+            bool ok = true;
+            if (issue_sd) {
+                ok = wait_bar(bar(B_KV), 0, abort_flag, p.err);
+                if (ok) ok = wait_bar(bar_full(0), 0, abort_flag, p.err);
+                if (ok) {
+                    ptx::tc_fence_after();
+                    gemm_sd(tm_buf0 + 128 * xb(0), sK, sbase + C::OFF_Q);
+                    ptx::mma_commit(bar(B_S_FULL + sp_slot(0)));
+                    gemm_sd(tm_buf0 + 128 * yb(0), sV, sbase + C::OFF_DO);
+                    ptx::mma_commit(bar(B_DP_FULL));
+                }
             }
             for (int it = 0; ok && it < n_it; ++it) {
                 const int s = it % C::STAGES;
@@ -340,14 +358,24 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
                 const uint32_t sQ = sbase + C::OFF_Q + s * C::kTileQ_B;
                 const uint32_t sdO = sbase + C::OFF_DO + s * C::kTileQ_B;
                 const uint32_t sdS = sbase + C::OFF_DS + dt(it) * C::kdS_B;
-                if (NBUF == 3 && it + 1 < n_it) {
-                    // S(i+1) into yb(i-1) once Q(i+1) is in and the dK product of iteration
-                    // i-1 stopped reading dS(i-1) from it (the first iteration's is unused)
-                    if (!(ok = wait_bar(bar_full(s1), ((it + 1) / C::STAGES) & 1, abort_flag, p.err))) break;
-                    if (it > 0 && !(ok = wait_bar(bar(B_G4), (it - 1) & 1, abort_flag, p.err))) break;
-                    ptx::tc_fence_after();
-                    gemm_sd(tm_buf0 + 128 * xb(it + 1), sK, sbase + C::OFF_Q + s1 * C::kTileQ_B);
-                    ptx::mma_commit(bar(B_S_FULL + sp_slot(it + 1)));
+                if (NBUF == 3 && issue_sd) {
+                    if (it + 1 < n_it) {
+                        // S(i+1) into yb(i-1) once Q(i+1) is in and the dK product of iteration
+                        // i-1 stopped reading dS(i-1) from it (the first iteration's is unused)
+                        if (!(ok = wait_bar(bar_full(s1), ((it + 1) / C::STAGES) & 1, abort_flag, p.err))) break;
+                        if (it > 0 &&
+                            !(ok = wait_bar(bar(B_YFREE + yb(it - 1)), ((it - 1) / 3) & 1, abort_flag, p.err)))
+                            break;
+                        ptx::tc_fence_after();
+                        gemm_sd(tm_buf0 + 128 * xb(it + 1), sK, sbase + C::OFF_Q + s1 * C::kTileQ_B);
+                        ptx::mma_commit(bar(B_S_FULL + sp_slot(it + 1)));
+                        // dP(i+1) into xb(i) once dQ(i) left it
+                        if (!(ok = wait_bar(bar(B_DQ_EMPTY), it & 1, abort_flag, p.err))) break;
+                        ptx::tc_fence_after();
+                        gemm_sd(X, sV, sbase + C::OFF_DO + s1 * C::kTileQ_B);
+                        ptx::mma_commit(bar(B_DP_FULL));
+                    }
+                    continue;
                 }
                 // dV += P^T dO.  A = P^T in TMEM: queries [0,64) packed in X[0,32), queries
                 // [64,128) in X[64,96); 16 queries = 8 packed columns per step.
@@ -373,19 +401,18 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
                 for (int k = 0; k < BM / 16; ++k)
                     ptx::mma_ts(tmem + C::TM_DK, Y + packed_col(k), ptx::sw128_desc(sQ + k * 2048, C::kBoxQ_B, 1024),
                                 ID_KV, (it > 0 || k > 0) ? 1u : 0u);
-                ptx::mma_commit(bar(B_G4));
-                // Q(i), dO(i) no longer read by MMAs (for d = 128 the stage is free only once
-                // the drain also arrived: it stages half of dQ(i) in the dO tile)
+                ptx::mma_commit(bar(NBUF == 3 ? B_YFREE + yb(it) : B_G4));
+                // Q(i), dO(i) no longer read by MMAs (S(i) and dP(i) completed before dS(i);
+                // for d = 128 the stage is free only once the drain also arrived: it stages
+                // half of dQ(i) in the dO tile)
                 ptx::mma_commit(bar_empty(s));
-                if (it + 1 < n_it) {
-                    if (NBUF == 2) {
-                        // S(i+1) into Y once the dK product stopped reading dS(i) from it
-                        if (!(ok = wait_bar(bar_full(s1), ((it + 1) / C::STAGES) & 1, abort_flag, p.err))) break;
-                        if (!(ok = wait_bar(bar(B_G4), it & 1, abort_flag, p.err))) break;
-                        ptx::tc_fence_after();
-                        gemm_sd(Y, sK, sbase + C::OFF_Q + s1 * C::kTileQ_B);
-                        ptx::mma_commit(bar(B_S_FULL + sp_slot(it + 1)));
-                    }
+                if (NBUF == 2 && it + 1 < n_it) {
+                    // S(i+1) into Y once the dK product stopped reading dS(i) from it
+                    if (!(ok = wait_bar(bar_full(s1), ((it + 1) / C::STAGES) & 1, abort_flag, p.err))) break;
+                    if (!(ok = wait_bar(bar(B_G4), it & 1, abort_flag, p.err))) break;
+                    ptx::tc_fence_after();
+                    gemm_sd(Y, sK, sbase + C::OFF_Q + s1 * C::kTileQ_B);
+                    ptx::mma_commit(bar(B_S_FULL + sp_slot(it + 1)));
                     // dP(i+1) into X once dQ(i) left it
                     if (!(ok = wait_bar(bar(B_DQ_EMPTY), it & 1, abort_flag, p.err))) break;
                     ptx::tc_fence_after();
@@ -393,10 +420,11 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
                     ptx::mma_commit(bar(B_DP_FULL));
                 }
             }
-            ptx::mma_commit(bar(B_ACC));
-            // no MMA may still write TMEM when it is released
-            ptx::mma_commit(bar(B_FINAL));
-            drain_wait(bar(B_FINAL), 0);
+            if (issue_g) ptx::mma_commit(bar(B_ACC));
+            // no MMA of this thread may still write TMEM when it is released
+            const int fin = issue_g ? B_FINAL : B_FINAL_A;
+            ptx::mma_commit(bar(fin));
+            drain_wait(bar(fin), 0);
         }
         __syncwarp();
     } else if (warp >= kWarpSoft0 && warp < kWarpSoft0 + kNumSoftWarps) {
@@ -619,7 +647,7 @@ __global__ void __launch_bounds__(threads_for(kDet), 1)
             }
         }
         if (!det && t == 0) ptx::bulk_wait_all();
-    } else if (warp == kWarpRed) {
+    } else if (warp == red_warp(D)) {
         // ------------------------------------------------------------ deterministic dQ adds
         // One thread waits for each staged dQ(i), takes the tile's turn, issues the
         // reduce-adds and passes the turn on once they are complete, so none of these waits
@@ -756,7 +784,7 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, const void* dO
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
     const long grid = (long)((s.S_k + BN - 1) / BN) * s.B * s.H_kv;
-    kern<<<(unsigned)grid, threads_for(ws.dq_sem != nullptr), C::SMEM, st>>>(tq, tk, tv, tdo, tdq, p);
+    kern<<<(unsigned)grid, threads_for(ws.dq_sem != nullptr, D), C::SMEM, st>>>(tq, tk, tv, tdo, tdq, p);
     return cudaGetLastError();
 }
 
