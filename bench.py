@@ -153,9 +153,12 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def main_kernel_traffic(workload: str):
+def main_kernel_traffic(workload: str, deterministic: bool = False):
     """DRAM bytes (read + write) per main-kernel launch from the committed ncu summary, or None
-    when the kernel's sources changed since the counters were taken."""
+    when the kernel's sources changed since the counters were taken.  The counters are those of
+    the default (non-deterministic) kernel instance: a deterministic run gets None."""
+    if deterministic:
+        return None
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -363,10 +366,11 @@ def main():
     main_ms = ms_main / max(calls, 1)
     achieved = flops / (main_ms / 1e3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    traffic = main_kernel_traffic(w.name)
+    traffic = main_kernel_traffic(w.name, det)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic, "peak_source": f"{peak_src} bf16_tflops (burst)",
-                "kernel": f"bwd_sm103_kernel<{w.dtype},{w.d}>", "kernel_ms": main_ms,
+                "kernel": f"bwd_sm103_kernel<{w.dtype},{w.d},{'det' if det else 'default'}>",
+                "kernel_ms": main_ms,
                 "preprocess_ms": ms_pre / max(calls, 1), "finalize_ms": ms_fin / max(calls, 1),
                 "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", 1700.0)),
                 "step_frac": (flops / (ms / 1e3) / 1e12) / peak}
