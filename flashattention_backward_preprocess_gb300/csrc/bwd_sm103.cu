@@ -1,5 +1,5 @@
 // bwd_sm103.cu -- FlashAttention-2 backward main kernel for GB300 (sm_103a),
-// f16 / bf16 inputs, head dim 64 or 128.
+// f16 / bf16 inputs, head dim 64 or 128 (32 and 96 run these with zero-filled columns).
 //
 // Math (the chain rule of O = softmax(scale Q K^T) V, with the saved LSE as
 // the softmax normaliser and D from the preprocess step; boostr
@@ -12,14 +12,16 @@
 // Design (Blackwell-native, not the pages' one-thread-per-key-row design):
 //   * one CTA owns a 128-row key/value tile of one (batch, kv head) and walks
 //     every 128-row query tile of every query head of the group, so dK and dV
-//     of the group are summed in tensor memory without atomics;
+//     of the group are summed in tensor memory without atomics.  Causal calls
+//     start the heaviest key tiles first; non-causal and windowed calls run the
+//     groups in blocks of 4 (L2 locality of the dQ adds and the Q / dO reads);
 //   * the five per-tile products run on the 5th-generation tensor cores
 //     (tcgen05.mma, M = 128, fp32 accumulation in TMEM).  S^T and dP^T are
 //     computed "key-major" (TMEM lane = key row), so the softmax-gradient
 //     threads own one key row each and write P^T / dS^T back into TMEM, packed
 //     to 16 bits, as the A operand of the dV / dK products;
 //   * TMA (cp.async.bulk.tensor, 128-byte swizzle) stages K, V once and Q, dO
-//     in a multi-stage ring; causal tiles that no query can see are skipped;
+//     in a multi-stage ring; tiles that no query can see are skipped;
 //   * the dQ tile (dS K) is drained from TMEM and added to the fp32
 //     accumulator in global memory with TMA bulk reduce-adds, staged through
 //     the dS shared-memory tile (free once the dQ product ran) and, for d = 128,
@@ -27,20 +29,23 @@
 //   * warp roles: warps 0-3 drain dQ; warps 4-11 compute P and dS and run the
 //     dK / dV epilogue, two warps per TMEM lane quadrant (one per 64-query half,
 //     so each SM sub-partition has two of them to hide TMEM / shared latency);
-//     warp 12 issues TMA; warp 13 owns TMEM and issues MMAs;
-//   * two 128-column TMEM buffers alternate roles each iteration i:
-//       X = buffer[i & 1]:  S(i) -> P(i) (packed) -> dQ(i)
-//       Y = buffer[~i & 1]: dP(i) -> dS(i) (packed in place) -> S(i+1)
-//     where "packed" puts queries [0,64) in columns [0,32) and queries [64,128)
-//     in columns [64,96) of the buffer
-//     (Y becomes X of the next iteration); the dQ product is issued first once
+//     warp 12 issues TMA; warp 13 owns TMEM and issues MMAs (at d = 64 the S and
+//     dP products, warp 14 the dV, dQ and dK products); the deterministic
+//     instance adds one warp that takes the dQ turns and issues the reduce-adds;
+//   * 128-column TMEM buffers take the roles X(i): S(i) -> P(i) (packed) -> dQ(i)
+//     and Y(i): dP(i) -> dS(i) (packed in place), where "packed" puts queries
+//     [0,64) in columns [0,32) and queries [64,128) in columns [64,96).  Two
+//     buffers at d = 128 (Y(i) becomes X(i+1): S(i+1) waits for the dK product
+//     of iteration i); three at d = 64, where S(i+1) goes into Y(i-1) and runs
+//     while the softmax warps still work on iteration i.  dP(i+1) always goes
+//     into X(i) once dQ(i) has been drained; the dQ product is issued first once
 //     dS(i) is ready, so its drain starts as early as possible;
 //   * every mbarrier wait is bounded: on timeout the kernel records an error
 //     word, lets the other roles drop out, waits for its own copies / MMAs in
 //     flight, frees TMEM and returns.
 //
-// TMEM columns (512 allocated): dV [0, D), dK [D, 2D), buffer 0 [2D, 2D+128),
-// buffer 1 [2D+128, 2D+256).
+// TMEM columns (512 allocated): dV [0, D), dK [D, 2D), buffers from 2D, 128
+// columns each (two at D = 128, three at D = 64).
 #include <math.h>
 
 #include "bounded_wait.cuh"

@@ -95,7 +95,8 @@ __host__ __device__ __forceinline__ void key_range(const Shape& s, int i0, int i
 
 // Head dims the library takes.  The CUDA-core kernels and the preprocess are instantiated
 // for each; the tensor-core kernels run d = 32 and 96 as d = 64 and 128 with the missing
-// columns zero-filled by TMA (their global extents and strides stay d), d = 256 on CUDA cores.
+// columns zero-filled by TMA (their global extents and strides stay d); at d = 256 the
+// forward has a tensor-core instance of its own and the backward runs on CUDA cores.
 #define FA_FOR_DTYPE(dtype, DD, CALL)              \
     do {                                           \
         if ((dtype) == FA_F32) CALL(float, DD);    \
@@ -114,7 +115,8 @@ __host__ __device__ __forceinline__ void key_range(const Shape& s, int i0, int i
         }                                                         \
     } while (0)
 inline bool head_dim_supported(int d) { return d == 32 || d == 64 || d == 96 || d == 128 || d == 256; }
-// The tensor-core kernels' compiled head dim for a call's d (0: none, CUDA cores instead).
+// The tensor-core backward's compiled head dim for a call's d (0: none, CUDA cores instead);
+// the forward adds d = 256.
 inline int tc_head_dim(int d) { return d == 32 || d == 64 ? 64 : (d == 96 || d == 128 ? 128 : 0); }
 
 // Device error word codes (bit set by a kernel whose bounded wait ran out).

@@ -1,19 +1,21 @@
-// fwd_sm103.cu -- attention forward for GB300 (sm_103a), f16 / bf16, head dim 64
-// or 128: the O and LSE the backward consumes (boostr autograd_attention.rs: the
+// fwd_sm103.cu -- attention forward for GB300 (sm_103a), f16 / bf16, head dim 64,
+// 128 or 256 (32 and 96 run the 64 / 128 kernels with zero-filled columns): the O
+// and LSE the backward consumes (boostr autograd_attention.rs: the
 // forward saves q, k, v, output and lse for FlashAttentionBackward).
 //
 //   s_ij = scale <Q_i, K_j> over the visible keys j (key_visible: causal keeps
 //          j <= i + S_k - S_q, a sliding window a band around that position)
 //   O_i  = sum_j exp(s_ij) V_j / sum_j exp(s_ij),   LSE_i = log sum_j exp(s_ij)
-// computed with the online softmax over 128-key tiles; a row that sees no key
+// computed with the online softmax over 128-key tiles (64-key at d = 256); a row that sees no key
 // gets O = 0 and LSE = -inf.
 //
 // Design:
 //   * one CTA per (128-row query tile, query head); the query tiles with the most
 //     visible key tiles start first;
 //   * S = Q K^T for key tile j runs on the 5th-generation tensor cores into one of
-//     three 128-column TMEM buffers, so S(j+1) and S(j+2) are computed while the
-//     softmax warps work on S(j); P = exp2(x - m) is packed to 16 bits in place and
+//     three 128-column TMEM buffers (two at d = 256, whose O takes columns
+//     [256, 512)), so S(j+1) and S(j+2) are computed while the softmax warps work
+//     on S(j); P = exp2(x - m) is packed to 16 bits in place and
 //     is the TMEM A operand of O += P V (O accumulates in TMEM, fp32);
 //   * one softmax thread per query row (TMEM lane), logits handled in log2 units
 //     x = s * log2(e).  The running max m moves only when a tile's max exceeds it

@@ -72,7 +72,8 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
-// tma_reduce_add_3d with an L2 cache policy for the lines it updates
+// Element-wise add of a shared-memory box into global memory through a tensor map
+// (cp.reduce.async.bulk.tensor), with an L2 cache policy for the lines it updates
 __device__ __forceinline__ void tma_reduce_add_3d_hint(const CUtensorMap* map, uint32_t src, int c0, int c1,
                                                        int c2, uint64_t pol) {
     asm volatile(
@@ -197,15 +198,6 @@ __device__ __forceinline__ void tmem_ld32p(uint32_t taddr, uint32_t* r) {
 }
 
 // ---------------------------------------------------------------- bulk reductions
-// Element-wise add of a shared-memory box into global memory through a tensor map.
-__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int c0, int c1,
-                                                  int c2) {
-    asm volatile(
-        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
-        " [%0, {%1, %2, %3}], [%4];" ::"l"(reinterpret_cast<uint64_t>(map)),
-        "r"(c0), "r"(c1), "r"(c2), "r"(src)
-        : "memory");
-}
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
