@@ -13,9 +13,10 @@ at a random later time.  It checks that
   * every wait sees its barrier either at the awaited phase (blocks) or one past it (passes),
   * no schedule deadlocks,
   * every read of a TMEM buffer or shared tile finds the data the reader expects.
-It covers the configurations the kernel has: two TMEM buffers and one MMA issuer (d = 128), three
+It covers the configurations the backward has: two TMEM buffers and one MMA issuer (d = 128), three
 buffers, two dS tiles and two issuers (d = 64), each with the drain's first thread or (the
-deterministic instance) a reduce warp issuing the dQ reduce-adds.
+deterministic instance) a reduce warp issuing the dQ reduce-adds; and the forward kernel
+(csrc/fwd_sm103.cu) with three S buffers (d <= 128) or two (d = 256).
 
 The model is not generated from the kernel: a change to the kernel's protocol needs the same change
 here, and this test then says whether the new protocol is sound.
@@ -267,8 +268,7 @@ class Model:
             yield self.wait(f"DQ_STAGED{self.dt(it)}", it // self.NDS)
             yield from self.reduce_staged(it)
 
-    # ---- scheduler
-    def run(self):
+    def make_roles(self):
         roles = {"producer": self.producer(), "softmax": self.softmax(), "drain": self.drain()}
         if self.n > 0:
             if self.split:
@@ -278,6 +278,11 @@ class Model:
                 roles["mma"] = self.issuer_single()
         if self.use_red:
             roles["reducer"] = self.reducer()
+        return roles
+
+    # ---- scheduler
+    def run(self):
+        roles = self.make_roles()
         blocked = {name: None for name in roles}  # pending request of each role
         for name in list(roles):
             self.advance(roles, blocked, name, None)
@@ -340,7 +345,7 @@ class Model:
                 return
             if req[0] == "arrive":
                 self.bars[req[1]].arrive()
-            elif req[0] in ("mma", "commit"):
+            elif req[0] in ("mma", "mma_pv", "commit"):
                 self.mma_q.setdefault(req[1], []).append(req)
             else:
                 raise AssertionError(req)
@@ -489,3 +494,137 @@ def test_model_reads_one_threads_mmas_in_order():
                 yield req
 
     assert not _fails(NoG4, 128, False, trials=100)
+
+
+class FwdModel(Model):
+    """One CTA of the tensor-core forward (csrc/fwd_sm103.cu) over n key tiles: a TMA warp
+    (Q once, K / V through a ring), a warp issuing S(j) = Q K(j)^T into TMEM buffer j % NB, a warp
+    issuing O += P(j) V(j) from that buffer, and the softmax warps (one actor here), which turn
+    S(j) into P(j) in place, sometimes rescale the O rows in TMEM (after P V(j-1) completed) and
+    finally read O.  NB = 3 S buffers for d <= 128, 2 for d = 256."""
+
+    def __init__(self, n_tiles, d, rng):
+        self.n, self.rng, self.d = n_tiles, rng, d
+        self.NB = 3 if d <= 128 else 2
+        self.STAGES = {64: 4, 128: 3, 256: 2}[d]
+        self.bars = {}
+        for name in ("Q", "FINAL"):
+            self.bars[name] = Bar(name, 1)
+        for k in range(3):
+            for kind in ("S", "P", "PV"):
+                self.bars[f"{kind}{k}"] = Bar(f"{kind}{k}", 1)
+        for st in range(self.STAGES):
+            self.bars[f"FULL{st}"] = Bar(f"FULL{st}", 1)
+            self.bars[f"EMPTY{st}"] = Bar(f"EMPTY{st}", 1)
+        self.res = {"O": 0}      # O: number of P V products accumulated
+        self.mma_q, self.async_ops, self.async_done, self.handle = {}, [], set(), 0
+
+    def make_roles(self):
+        roles = {"tma": self.f_tma(), "softmax": self.f_softmax()}
+        if self.n > 0:
+            roles["s_issuer"] = self.f_s_issuer()
+            roles["pv_issuer"] = self.f_pv_issuer()
+        return roles
+
+    def f_tma(self):
+        self.async_ops.append(("tma", [("Qt", "Q")], "Q"))
+        for j in range(self.n):
+            st = j % self.STAGES
+            if j >= self.STAGES:
+                yield self.wait(f"EMPTY{st}", j // self.STAGES - 1)
+            self.async_ops.append(("tma", [(f"K{st}", ("K", j)), (f"V{st}", ("V", j))], f"FULL{st}"))
+
+    def f_s_issuer(self):
+        yield self.wait("Q", 0)
+        for j in range(self.n):
+            st, b = j % self.STAGES, j % self.NB
+            yield self.wait(f"FULL{st}", j // self.STAGES)
+            if j >= self.NB:  # P V(j - NB) has read P out of buffer b
+                yield self.wait(f"PV{b}", j // self.NB - 1)
+            yield ("mma", "S", [("Qt", "Q"), (f"K{st}", ("K", j))], [(f"sbuf{b}", ("S", j))])
+            yield ("commit", "S", f"S{b}")
+
+    def f_pv_issuer(self):
+        for j in range(self.n):
+            st, b = j % self.STAGES, j % self.NB
+            yield self.wait(f"P{b}", j // self.NB)
+            yield ("mma_pv", "PV", j, b, st)
+            yield ("commit", "PV", f"PV{b}")
+            yield ("commit", "PV", f"EMPTY{st}")  # S(j) completed before P(j)
+        yield ("commit", "PV", "FINAL")
+        yield self.wait("FINAL", 0)
+
+    def f_softmax(self):
+        for j in range(self.n):
+            b = j % self.NB
+            yield self.wait(f"S{b}", j // self.NB)
+            self.expect(f"sbuf{b}", ("S", j))
+            yield self.STEP
+            self.put(f"sbuf{b}", ("P", j))
+            if j > 0 and self.rng.random() < 0.5:  # the running max moved: rescale O
+                yield self.wait(f"PV{(j - 1) % self.NB}", (j - 1) // self.NB)
+                self.expect("O", j)
+                yield self.STEP
+                self.expect("O", j)
+            yield self.arrive(f"P{b}")
+        if self.n > 0:
+            yield from self.f_epilogue()
+        self.expect("O", self.n)
+
+    def f_epilogue(self):
+        yield self.wait("FINAL", 0)
+
+    def exec_mma(self, who):
+        op = self.mma_q[who][0]
+        if op[0] == "mma_pv":
+            self.mma_q[who].pop(0)
+            _, _, j, b, st = op
+            self.expect(f"sbuf{b}", ("P", j))
+            self.expect(f"V{st}", ("V", j))
+            self.expect("O", j)
+            self.put("O", j + 1)
+            return
+        super().exec_mma(who)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_forward_protocol_sound_under_random_schedules(d):
+    rng = random.Random(2000 + d)
+    for _ in range(400):
+        FwdModel(rng.choice([1, 2, 3, 4, 5, 7, 9]), d, random.Random(rng.random())).run()
+
+
+def test_forward_model_catches_one_shared_pv_barrier():
+    # one P V barrier for all S buffers (the design before the per-buffer ones): a parity wait
+    # for P V(j) can see the barrier a phase behind (P V(j-1) pending: the old epilogue read O
+    # early) or ahead
+    class SharedPV(FwdModel):
+        def f_s_issuer(self):
+            for req in super().f_s_issuer():
+                if req[0] == "wait" and req[1].startswith("PV"):
+                    req = self.wait("PV0", req[2] * self.NB + int(req[1][2:]))
+                yield req
+
+        def f_pv_issuer(self):
+            for req in super().f_pv_issuer():
+                if req[0] == "commit" and req[2].startswith("PV"):
+                    req = ("commit", req[1], "PV0")
+                yield req
+
+        def f_softmax(self):
+            for req in super().f_softmax():
+                if req[0] == "wait" and req[1].startswith("PV"):
+                    req = self.wait("PV0", req[2] * self.NB + int(req[1][2:]))
+                yield req
+
+        def f_epilogue(self):
+            yield self.wait("PV0", self.n - 1)
+
+    rng = random.Random(5)
+    caught = 0
+    for _ in range(400):
+        try:
+            SharedPV(rng.choice([4, 5, 7]), 128, random.Random(rng.random())).run()
+        except ProtocolError:
+            caught += 1
+    assert caught > 0
