@@ -280,6 +280,8 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
         return rc;
     const Shape s = make_shape(B, H, H_kv, S_q, S_k, d, scale, causal, window);
     cudaError_t e;
+    // f16 / bf16: the tensor-core forward at every supported head dim (d = 256 with 64-key
+    // tiles); f32 (and FA_FWD_KERNEL=simt): the CUDA-core helper
     if (dtype == FA_F32 || fwd_simt_for_16bit()) {
         e = launch_fwd_simt(dtype, Q, K, V, O, LSE, s, st);
     } else {
