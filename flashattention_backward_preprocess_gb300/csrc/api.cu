@@ -56,7 +56,8 @@ WsLayout ws_layout(int B, int H, int S_q, int d) {
     L.off_D = align_up(L.off_lse2 + rows_pad * 4, 256);
     L.off_dq = align_up(L.off_D + rows_pad * 4, 256);
     L.off_sem = align_up(L.off_dq + (size_t)B * H * S_q * d * 4, 256);
-    L.sem_bytes = (size_t)B * H * ((S_q + kTileQ - 1) / kTileQ) * 4;
+    // turn counters, then the CTA ticket counter
+    L.sem_bytes = ((size_t)B * H * ((S_q + kTileQ - 1) / kTileQ) + 1) * 4;
     L.total = align_up(L.off_sem + L.sem_bytes, 256);
     return L;
 }
@@ -230,10 +231,11 @@ int bwd_impl(const void* dO, const void* Q, const void* K, const void* V, const 
     ws.Dws = reinterpret_cast<float*>(static_cast<char*>(base) + L.off_D);
     ws.dqacc = reinterpret_cast<float*>(static_cast<char*>(base) + L.off_dq);
     ws.dq_sem = nullptr;
-    // tensor cores for f16 / bf16 at head dims up to 128; CUDA cores for f32 and d = 256
-    const bool tc = dtype != FA_F32 && !use_simt_for_16bit() && tc_head_dim(d) != 0;
+    ws.dq_ticket = nullptr;
+    const bool tc = bwd_uses_tensor_cores(dtype, d);
     if (deterministic && tc) {
         ws.dq_sem = reinterpret_cast<unsigned int*>(static_cast<char*>(base) + L.off_sem);
+        ws.dq_ticket = ws.dq_sem + L.sem_bytes / 4 - 1;
         cudaError_t me = cudaMemsetAsync(ws.dq_sem, 0, L.sem_bytes, st);
         if (me != cudaSuccess) return cuda_fail("turn counter reset", me);
     }
@@ -328,6 +330,11 @@ int validate_bwd_args(const void* dO, const void* Q, const void* K, const void* 
 }
 
 int set_error(int status, const char* arg, const char* reason) { return fail(status, arg, reason); }
+
+// tensor cores for f16 / bf16 at head dims up to 128; CUDA cores for f32 and d = 256
+bool bwd_uses_tensor_cores(int dtype, int d) {
+    return dtype != FA_F32 && !use_simt_for_16bit() && tc_head_dim(d) != 0;
+}
 
 void clear_error() { g_last_error.clear(); }
 
@@ -508,16 +515,26 @@ int fa_check_device(void* stream) {
     {
         std::lock_guard<std::mutex> lk(g_ws_mu);
         auto it = g_ws.find({dev, st});
-        if (it == g_ws.end()) return FA_OK;
-        base = it->second.base;
+        if (it != g_ws.end()) base = it->second.base;
     }
     unsigned int words[4] = {0, 0, 0, 0};
-    e = cudaMemcpy(words, base, sizeof(words), cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return cuda_fail("cudaMemcpy", e);
-    if (words[0] == 0) return FA_OK;
-    cudaMemset(base, 0, sizeof(words));
-    if (words[0] & kErrTimeout) return fail(FA_ERR_TIMEOUT, "device", "a bounded wait in a kernel timed out");
-    return fail(FA_ERR_CUDA, "device", "kernel error word " + std::to_string(words[0]));
+    if (base != nullptr) {
+        e = cudaMemcpy(words, base, sizeof(words), cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return cuda_fail("cudaMemcpy", e);
+        if (words[0] != 0) {
+            e = cudaMemset(base, 0, sizeof(words));
+            if (e != cudaSuccess) return cuda_fail("cudaMemset", e);
+        }
+    }
+    // fa_bwd_noalloc records its timeouts in its own scratch, shared by every stream
+    unsigned int na_word = 0;
+    const int rc = noalloc_take_error_word(&na_word);
+    if (rc != FA_OK) return rc;
+    const int status = status_from_error_words(words[0], na_word);
+    if (status == FA_ERR_TIMEOUT) return fail(FA_ERR_TIMEOUT, "device", "a bounded wait in a kernel timed out");
+    if (status != FA_OK)
+        return fail(status, "device", "kernel error word " + std::to_string(words[0] | na_word));
+    return FA_OK;
 }
 
 int fa_profile(int enable) {

@@ -42,7 +42,7 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, vol
 
 // Bounded wait until a counter in global memory, advanced by other CTAs of the same launch
 // (release stores), reaches `want`; acquire ordering on success.  Polls every ~100 ns.
-// The CTAs waited for have lower block indices, so they were dispatched earlier.
+// The CTAs waited for took lower start-order tickets, so they are already running.
 __device__ __forceinline__ bool wait_counter(const unsigned int* ctr, unsigned int want,
                                              volatile int* abort_flag, unsigned int* err,
                                              uint64_t limit_ns = kWaitLimitNs) {

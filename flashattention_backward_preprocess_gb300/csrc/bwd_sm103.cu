@@ -128,6 +128,7 @@ struct Params {
     void* dV;
     unsigned int* err;
     unsigned int* dq_sem;  // deterministic dQ: [B*H][query tiles] turn counters, else nullptr
+    unsigned int* ticket;  // deterministic dQ: counter handing out logical CTA indices, else nullptr
     int B, H, H_kv, S_q, S_k, S_q_pad;
     int d;  // head dim of the tensors (<= D: columns d..D-1 are zero-filled by TMA, never stored)
     float scale, scale_log2;
@@ -173,21 +174,50 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
 
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 4);
+    uint32_t* ticket_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 8);
     auto bar = [&](int i) { return sbase + C::OFF_BAR + 8u * (uint32_t)i; };
     auto bar_full = [&](int s) { return bar(B_STAGE0 + s); };
     auto bar_empty = [&](int s) { return bar(B_STAGE0 + C::STAGES + s); };
 
-    // ---- work assignment: blockIdx.x = (block of group_chunk (b, kv head) groups) x key
-    // tile x (group within the block).  With one block of every group (causal) the heaviest
-    // key tiles (most query tiles) start first.  When every key tile sees about as many query
-    // tiles (no causal mask, or a sliding window) blocks of a few groups run one after the
-    // other instead, so that all key-tile CTAs of a group run side by side.  Each CTA walks
-    // its query tiles from the last one down, heads innermost: CTAs running side by side
-    // reduce into and read the same dQ / Q / dO tiles at about the same time.  Within a
-    // group a lower key tile always has a lower block index.
+    if (threadIdx.x == 0) {
+        if ((sbase & 1023u) != 0) atomicOr(p.err, kErrSmemAlign);
+        *abort_flag = (sbase & 1023u) != 0;
+        for (int i = 0; i < (int)C::kNumBars; ++i) {
+            uint32_t count = ((i >= B_P_READY && i < B_P_READY + 3) || i == B_DS_READY) ? (uint32_t)kNumSoftWarps
+                             : (i == B_DQ_EMPTY || i == B_DQ_STAGED || i == B_DQ_STAGED + 1) ? 4u
+                                                               : 1u;
+            if (D == 128 && i >= B_STAGE0 + C::STAGES) count = 2;  // stage "empty": MMA + drain
+            ptx::mbar_init(bar(i), count);
+        }
+        ptx::fence_mbar_init();
+        ptx::fence_proxy_async_smem();
+        if (kDet) *ticket_slot = atomicAdd(p.ticket, 1u);
+    }
+    if (warp == kWarpMma) {
+        ptx::tmem_alloc(sbase + C::OFF_MISC + 4, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tm_buf0 = tmem + C::TM_BUF0;  // buffer x at tm_buf0 + 128 * x
+
+    // ---- work assignment: logical index blk = (block of group_chunk (b, kv head) groups) x
+    // key tile x (group within the block).  blk is blockIdx.x, except in deterministic mode,
+    // where each CTA takes it from a ticket counter in the order the CTAs start: a CTA then
+    // only waits (for dQ turns) on CTAs of lower logical index, which have all started,
+    // whatever order the hardware dispatches blocks in.  With one block of every group
+    // (causal) the heaviest key tiles (most query tiles) start first.  When every key tile
+    // sees about as many query tiles (no causal mask, or a sliding window) blocks of a few
+    // groups run one after the other instead, so that all key-tile CTAs of a group run side
+    // by side.  Each CTA walks its query tiles from the last one down, heads innermost: CTAs
+    // running side by side reduce into and read the same dQ / Q / dO tiles at about the
+    // same time.  Within a group a lower key tile always has a lower logical index.
     const int n_key_tiles = (p.S_k + BN - 1) / BN;
-    const int chunk = blockIdx.x / (n_key_tiles * p.group_chunk);
-    const int in_chunk = blockIdx.x % (n_key_tiles * p.group_chunk);
+    const int blk = kDet ? (int)*ticket_slot : (int)blockIdx.x;
+    const int chunk = blk / (n_key_tiles * p.group_chunk);
+    const int in_chunk = blk % (n_key_tiles * p.group_chunk);
     const int n_tile = in_chunk / p.group_chunk;
     const int bkv = chunk * p.group_chunk + in_chunk % p.group_chunk;
     const int b = bkv / p.H_kv, hk = bkv % p.H_kv;
@@ -208,29 +238,6 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
     const int m_end = q_hi > q_lo ? (q_hi + BM - 1) / BM : m_start;
     const int nm = m_end - m_start;
     const int n_it = g * nm;
-
-    if (threadIdx.x == 0) {
-        if ((sbase & 1023u) != 0) atomicOr(p.err, kErrSmemAlign);
-        *abort_flag = (sbase & 1023u) != 0;
-        for (int i = 0; i < (int)C::kNumBars; ++i) {
-            uint32_t count = ((i >= B_P_READY && i < B_P_READY + 3) || i == B_DS_READY) ? (uint32_t)kNumSoftWarps
-                             : (i == B_DQ_EMPTY || i == B_DQ_STAGED || i == B_DQ_STAGED + 1) ? 4u
-                                                               : 1u;
-            if (D == 128 && i >= B_STAGE0 + C::STAGES) count = 2;  // stage "empty": MMA + drain
-            ptx::mbar_init(bar(i), count);
-        }
-        ptx::fence_mbar_init();
-        ptx::fence_proxy_async_smem();
-    }
-    if (warp == kWarpMma) {
-        ptx::tmem_alloc(sbase + C::OFF_MISC + 4, kTmemCols);
-        ptx::tmem_relinquish();
-    }
-    ptx::tc_fence_before();
-    __syncthreads();
-    ptx::tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t tm_buf0 = tmem + C::TM_BUF0;  // buffer x at tm_buf0 + 128 * x
 
     // Buffer roles.  Iteration i computes S(i) -> P(i) -> dQ(i) in buffer xb(i) and
     // dP(i) -> dS(i) in buffer yb(i); dP(i+1) always goes into xb(i) once dQ(i) left it.
@@ -674,7 +681,7 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
                 // tile (they are consecutive: the first is where key_range of the query tile
                 // starts).  Wait for the turn, add, and pass it on once the adds are complete:
                 // one iteration later, so this thread never waits for its newest reduce.  Holding
-                // that turn meanwhile cannot deadlock: only CTAs of higher block index wait
+                // that turn meanwhile cannot deadlock: only CTAs of higher logical index wait
                 // for it, and this CTA never waits for one of those.
                 int k_lo, k_hi;
                 key_range(sh, m0, min(m0 + BM, p.S_q), k_lo, k_hi);
@@ -764,6 +771,7 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, const void* dO
     p.dV = dV;
     p.err = ws.err;
     p.dq_sem = ws.dq_sem;
+    p.ticket = ws.dq_ticket;
     p.B = s.B;
     p.H = s.H;
     p.H_kv = s.H_kv;

@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "error_words.h"
 #include "fa.h"  // include/fa.h (nvcc -I include)
 
 namespace fa {
@@ -119,12 +120,6 @@ inline bool head_dim_supported(int d) { return d == 32 || d == 64 || d == 96 || 
 // the forward adds d = 256.
 inline int tc_head_dim(int d) { return d == 32 || d == 64 ? 64 : (d == 96 || d == 128 ? 128 : 0); }
 
-// Device error word codes (bit set by a kernel whose bounded wait ran out).
-enum : unsigned int {
-    kErrTimeout = 1u,
-    kErrSmemAlign = 2u,
-};
-
 // Library-owned scratch for one fa_bwd call (device memory).
 struct Workspace {
     unsigned int* err;  // [4] error words
@@ -134,6 +129,9 @@ struct Workspace {
     // [B*H][ceil(S_q / 128)] turn counters of the deterministic dQ reduction (zeroed per
     // call), or nullptr: then dQ tiles are reduced in whatever order the CTAs reach them
     unsigned int* dq_sem;
+    // deterministic dQ: the counter (zeroed with dq_sem) from which the CTAs take their
+    // logical indices in start order; nullptr otherwise
+    unsigned int* dq_ticket;
 };
 
 constexpr int kTileQ = 128;  // query rows per main-kernel iteration
@@ -172,5 +170,14 @@ int validate_bwd_args(const void* dO, const void* Q, const void* K, const void* 
                       int H_kv, int S_q, int S_k, int d, float scale, int causal, int dtype);
 int set_error(int status, const char* arg, const char* reason);
 void clear_error();
+// True when fa_bwd runs the tcgen05 kernel for this dtype and head dim (f16 / bf16 at a
+// head dim the tensor-core backward takes, unless FA_BWD_KERNEL=simt); every backward
+// entry point picks its main kernel with this one test.
+bool bwd_uses_tensor_cores(int dtype, int d);
+
+// noalloc.cu: reads the error word of the no-allocation scratch on the current device
+// into *word and clears it (0 if fa_bwd_noalloc never ran on this device).  Returns an
+// fa_status.
+int noalloc_take_error_word(unsigned int* word);
 
 }  // namespace fa

@@ -17,14 +17,18 @@
 //     (each part rounded up to 256); larger shapes are rejected with
 //     FA_ERR_INVALID_ARG ("scratch: ...") and nothing is launched.
 //   * The first call on a device looks up the array's device address
-//     (cudaGetSymbolAddress) and clears its error words; make that first call
-//     before any stream capture.
+//     (cudaGetSymbolAddress, which may load the library's device code) and
+//     enqueues the clearing of its error words on the caller's stream; make
+//     that first call before any stream capture.
 //   * All calls share the one array and it keeps the last call's contents;
 //     every call re-zeroes the parts that must start at zero.  Calls whose GPU
 //     work overlaps (other streams, other host threads) race on it: order them
 //     on one stream.
 //   * Device-side bounded-wait timeouts of this variant are recorded in the
-//     array's first word, which fa_check_device does not read.
+//     array's first word; fa_check_device reads and clears it (after
+//     synchronizing the stream it is given, so pass the stream of the calls).
+//   * The main kernel is chosen as fa_bwd chooses it (FA_BWD_KERNEL=simt
+//     included).
 #include <stdio.h>
 
 #include <mutex>
@@ -48,8 +52,10 @@ void* g_na_ptr[kFaMaxDevices] = {};
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Device address of the scratch array on the current device (set-up once per device).
-int scratch_address(void** out) {
+// Device address of the scratch array on the current device (set-up once per device: the
+// address lookup, then the clearing of the error words enqueued on `st`; the address is
+// published only once that clear is enqueued, so every later call finds clean words).
+int scratch_address(cudaStream_t st, void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return set_error(FA_ERR_CUDA, "cudaGetDevice", cudaGetErrorString(e));
@@ -60,8 +66,8 @@ int scratch_address(void** out) {
         e = cudaGetSymbolAddress(&p, g_fa_noalloc_scratch);
         if (e != cudaSuccess || p == nullptr)
             return set_error(FA_ERR_CUDA, "cudaGetSymbolAddress", cudaGetErrorString(e));
-        e = cudaMemset(p, 0, 256);  // error words
-        if (e != cudaSuccess) return set_error(FA_ERR_CUDA, "cudaMemset", cudaGetErrorString(e));
+        e = cudaMemsetAsync(p, 0, 256, st);  // error words
+        if (e != cudaSuccess) return set_error(FA_ERR_CUDA, "cudaMemsetAsync", cudaGetErrorString(e));
         g_na_ptr[dev] = p;
     }
     *out = g_na_ptr[dev];
@@ -69,6 +75,24 @@ int scratch_address(void** out) {
 }
 
 }  // namespace
+
+int noalloc_take_error_word(unsigned int* word) {
+    *word = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return set_error(FA_ERR_CUDA, "cudaGetDevice", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kFaMaxDevices) return FA_OK;
+    std::lock_guard<std::mutex> lk(g_na_mu);
+    if (g_na_ptr[dev] == nullptr) return FA_OK;  // never used on this device
+    e = cudaMemcpy(word, g_na_ptr[dev], sizeof(unsigned int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return set_error(FA_ERR_CUDA, "cudaMemcpy", cudaGetErrorString(e));
+    if (*word != 0) {
+        e = cudaMemset(g_na_ptr[dev], 0, sizeof(unsigned int));
+        if (e != cudaSuccess) return set_error(FA_ERR_CUDA, "cudaMemset", cudaGetErrorString(e));
+    }
+    return FA_OK;
+}
+
 }  // namespace fa
 
 using namespace fa;
@@ -93,8 +117,9 @@ extern "C" int fa_bwd_noalloc(const void* dO, const void* Q, const void* K, cons
                  total, kFaNoallocScratchBytes);
         return set_error(FA_ERR_INVALID_ARG, "scratch", msg);
     }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
     void* base = nullptr;
-    if ((rc = scratch_address(&base)) != FA_OK) return rc;
+    if ((rc = scratch_address(st, &base)) != FA_OK) return rc;
     char* b = static_cast<char*>(base);
     Workspace ws;
     ws.err = reinterpret_cast<unsigned int*>(b);
@@ -102,6 +127,7 @@ extern "C" int fa_bwd_noalloc(const void* dO, const void* Q, const void* K, cons
     ws.Dws = reinterpret_cast<float*>(b + off_D);
     ws.dqacc = reinterpret_cast<float*>(b + off_dq);
     ws.dq_sem = nullptr;
+    ws.dq_ticket = nullptr;
     Shape s;
     s.B = B;
     s.H = H;
@@ -113,12 +139,11 @@ extern "C" int fa_bwd_noalloc(const void* dO, const void* Q, const void* K, cons
     s.causal = causal;
     s.window = 0;
     s.S_q_pad = S_q_pad;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     // the preprocess pass also zeroes the dQ accumulator rows this call uses
     cudaError_t e = launch_preprocess(dtype, dO, O, LSE, ws.Dws, ws.lse2, ws.dqacc, s, S_q_pad, st);
     if (e != cudaSuccess) return set_error(FA_ERR_CUDA, "preprocess launch", cudaGetErrorString(e));
-    e = dtype != FA_F32 && tc_head_dim(d) != 0 ? launch_bwd_sm103(dtype, Q, K, V, dO, ws, dK, dV, s, st)
-                        : launch_bwd_simt(dtype, Q, K, V, dO, ws, dK, dV, s, false, st);
+    e = bwd_uses_tensor_cores(dtype, d) ? launch_bwd_sm103(dtype, Q, K, V, dO, ws, dK, dV, s, st)
+                                        : launch_bwd_simt(dtype, Q, K, V, dO, ws, dK, dV, s, false, st);
     if (e != cudaSuccess) return set_error(FA_ERR_CUDA, "main kernel launch", cudaGetErrorString(e));
     e = launch_dq_finalize(dtype, ws.dqacc, dQ, s, st);
     if (e != cudaSuccess) return set_error(FA_ERR_CUDA, "dq finalize launch", cudaGetErrorString(e));

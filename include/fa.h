@@ -124,9 +124,10 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int
  *                   atomicAdd accumulation), bits may vary between runs;
  *                   1 = bitwise reproducible dQ: F16/BF16 add each 128x128
  *                   dQ tile's per-key-tile contributions in key-tile order
- *                   (the CTAs pass a turn counter in the workspace along; a
- *                   CTA only ever waits for CTAs with lower block indices of
- *                   the same launch, and every wait is bounded); F32 computes
+ *                   (the CTAs pass a turn counter in the workspace along; each
+ *                   CTA takes its tile from a ticket counter in the order the
+ *                   CTAs start and only ever waits for CTAs that started
+ *                   before it, and every wait is bounded); F32 computes
  *                   dQ in its own kernel, each row summed over keys in index
  *                   order.  Other values give FA_ERR_INVALID_ARG.
  * dK and dV are bitwise reproducible in both modes.  Every other argument,
@@ -171,12 +172,14 @@ int fa_bwd_host(const void* dO, const void* Q, const void* K, const void* V, con
  *     scratch (parts rounded up to 256 bytes); beyond 32 MiB the call returns
  *     FA_ERR_INVALID_ARG ("scratch: ...") and launches nothing.
  *   * The first call on a device looks the array's device address up and
- *     clears its error words: make that first call before any stream capture.
+ *     enqueues the clearing of its error words on `stream`: make that first
+ *     call before any stream capture.
  *   * Every call shares the array (it keeps the last call's contents; each
  *     call re-zeroes what must start at zero).  Calls whose GPU work overlaps,
  *     e.g. on different streams, race: keep them in one stream's order.
- *   * Bounded-wait timeouts of this variant are not reported by
- *     fa_check_device.
+ *   * The main kernel is the one fa_bwd would run for the same arguments.
+ *   * Bounded-wait timeouts of this variant are recorded in the array and
+ *     reported (then cleared) by fa_check_device(stream), as for fa_bwd.
  */
 int fa_bwd_noalloc(const void* dO, const void* Q, const void* K, const void* V, const void* O,
                    const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv,
@@ -188,8 +191,9 @@ int fa_bwd_noalloc(const void* dO, const void* Q, const void* K, const void* V, 
 size_t fa_bwd_workspace_bytes(int B, int H, int S_q, int d);
 
 /* Synchronizes `stream`, then returns FA_ERR_TIMEOUT if a kernel of this
- * library on that stream recorded a bounded-wait timeout since the last
- * check (clearing the record), else FA_OK (or FA_ERR_CUDA). */
+ * library on that stream, or an fa_bwd_noalloc call on this device, recorded
+ * a bounded-wait timeout since the last check (clearing the record), else
+ * FA_OK (or FA_ERR_CUDA). */
 int fa_check_device(void* stream);
 
 /*

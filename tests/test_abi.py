@@ -97,10 +97,12 @@ def test_preprocess_and_fwd_validate(lib):
 
 def test_workspace_bytes(lib):
     # err words, padded LSE*log2e and D copies (rows padded to 128), fp32 dQ accumulator,
-    # one turn counter per (query head, 128-row query tile) for the deterministic dQ mode
+    # one turn counter per (query head, 128-row query tile) for the deterministic dQ mode and
+    # its CTA ticket counter (rounded up to 256 bytes)
     B, H, S, d = 4, 32, 2048, 128
     rows = B * H * S
-    assert fa.fa_bwd_workspace_bytes(B, H, S, d) == 256 + 2 * rows * 4 + rows * d * 4 + B * H * (S // 128) * 4
+    sem = (B * H * (S // 128) * 4 + 4 + 255) // 256 * 256
+    assert fa.fa_bwd_workspace_bytes(B, H, S, d) == 256 + 2 * rows * 4 + rows * d * 4 + sem
     B, H, S, d = 1, 2, 200, 64
     rows_pad = B * H * 256
     got = fa.fa_bwd_workspace_bytes(B, H, S, d)

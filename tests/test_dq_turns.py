@@ -4,17 +4,20 @@ In the deterministic instance of the tensor-core backward (csrc/bwd_sm103.cu) ev
 of a query head receives the contributions of the key tiles that see it in key-tile order: the
 tile has a turn counter (zeroed per call); the CTA of the t-th such key tile waits until the
 counter equals t, issues its bulk reduce-adds, and one iteration later, once those adds are
-complete, stores t + 1.  The kernel relies on two facts to be free of deadlock:
-  * a CTA only waits for CTAs of lower block index (key tile outer in the block index, and the
-    key tiles of a query tile are consecutive from key_range's first one), and
-  * CTAs are dispatched in block-index order, each starting when a resident one finishes,
-so the lowest unfinished CTA is always resident and never waits.
+complete, stores t + 1.  The kernel is free of deadlock by construction:
+  * a CTA takes its logical index (which key tile of which group it owns) from a ticket counter
+    in the workspace, in the order the CTAs actually start, whatever order the hardware
+    dispatches the blocks in, and
+  * a CTA only waits for CTAs of lower logical index (key tile outer in the logical index, and
+    the key tiles of a query tile are consecutive from key_range's first one),
+so every CTA waited for has started, and the lowest unfinished one never waits.
 
-This model runs that protocol with a limited number of resident CTAs, CTA pipelines that cannot
-stage the next dQ tile before their reduce warp released the previous staging area, and adds that
-complete at random later times, and checks that no schedule deadlocks and that every dQ tile
-receives its adds, completed, in key-tile order.  Planted mistakes (passing a turn on before the
-adds complete, waiting for a higher block index) are caught.
+This model runs that protocol with a limited number of resident CTAs dispatched in a random
+order, CTA pipelines that cannot stage the next dQ tile before their reduce warp released the
+previous staging area, and adds that complete at random later times, and checks that no schedule
+deadlocks and that every dQ tile receives its adds, completed, in key-tile order.  Planted
+mistakes (passing a turn on before the adds complete, waiting for a higher index, taking the
+logical index from the block index instead of the ticket) are caught.
 """
 import random
 
@@ -36,8 +39,10 @@ def query_tiles_seen(kt, n_tiles, causal):
 
 class TurnModel:
     def __init__(self, groups, heads, n_tiles, causal, resident, rng, release_early=False,
-                 wrong_order=False, ds_tiles=1):
+                 wrong_order=False, ds_tiles=1, shuffle_dispatch=False, ticket=True):
         self.rng = rng
+        self.shuffle_dispatch = shuffle_dispatch  # blocks dispatched in a random order
+        self.ticket = ticket                      # logical index from the start-order ticket
         self.release_early = release_early
         self.ds_tiles = ds_tiles
         # block index = key tile * groups + group (key tile outer)
@@ -89,7 +94,10 @@ class TurnModel:
     def run(self):
         n = len(self.ctas)
         gens, blocked = {}, {}
-        next_cta = 0
+        next_cta = 0  # blocks started so far (= the next ticket)
+        order = list(range(n))  # physical block dispatched k-th
+        if self.shuffle_dispatch:
+            self.rng.shuffle(order)
         complete = set()
         inflight = []   # (handle, tile, kt) adds in flight
         steps = 0
@@ -133,7 +141,9 @@ class TurnModel:
             if steps > 200000:
                 raise TurnError("no progress")
             while next_cta < n and len(gens) < self.resident:
-                start(next_cta)
+                # with the ticket the k-th started block owns logical CTA k; without it, the
+                # block owns the logical CTA of its own block index
+                start(next_cta if self.ticket else order[next_cta])
                 next_cta += 1
             choices = [("cta", c) for c in gens if ready(blocked[c])]
             choices += [("add", k) for k in range(len(inflight))]
@@ -159,7 +169,21 @@ def test_turns_add_in_key_tile_order_without_deadlock(causal, resident):
     rng = random.Random(31 + resident + 7 * causal)
     for _ in range(150):
         TurnModel(groups=2, heads=2, n_tiles=rng.choice([1, 2, 3, 4]), causal=causal,
-                  resident=resident, rng=random.Random(rng.random())).run()
+                  resident=resident, rng=random.Random(rng.random()), shuffle_dispatch=True).run()
+
+
+def test_model_catches_block_index_order_under_out_of_order_dispatch():
+    # without the ticket, a block dispatched early may own a late logical index and wait for a
+    # block that cannot become resident: caught as a deadlock on some schedule
+    rng = random.Random(5)
+    caught = 0
+    for _ in range(100):
+        try:
+            TurnModel(1, 1, 4, False, 2, random.Random(rng.random()), shuffle_dispatch=True,
+                      ticket=False).run()
+        except TurnError:
+            caught += 1
+    assert caught > 0
 
 
 def test_model_catches_a_turn_passed_before_the_adds_complete():

@@ -41,6 +41,9 @@ def _call(lib, w, dO, Q, K, V, O, LSE, dQ, dK, dV):
 @pytest.mark.parametrize("w", [
     Workload("noalloc_bf16", "bf16", 1, 4, 2, 300, 300, 128, True, seed=31),
     Workload("noalloc_f16", "f16", 2, 2, 1, 200, 333, 64, False, seed=32),
+    # the other main kernels through the same scratch: fp32, and head dim 256
+    Workload("noalloc_f32", "f32", 1, 4, 2, 200, 200, 128, True, seed=33),
+    Workload("noalloc_bf16_d256", "bf16", 1, 2, 1, 300, 300, 256, True, seed=34),
 ], ids=lambda w: w.name)
 def test_noalloc_matches_fa_bwd_on_two_calls(w):
     lib = fa.load_library()
@@ -57,6 +60,7 @@ def test_noalloc_matches_fa_bwd_on_two_calls(w):
         for name, got, r in zip(("dQ", "dK", "dV"), out, ref):
             assert bool(torch.isfinite(got).all()), name
             assert _rel(got, r) <= TOL[w.dtype], (name, _rel(got, r))
+    fa.fa_check_device()  # no bounded wait of either entry point ran out
 
 
 @pytest.mark.gpu
