@@ -18,7 +18,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libfa.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "preprocess.cu", "bwd_simt.cu", "fwd_simt.cu", "fwd_sm103.cu", "bwd_sm103.cu", "noalloc.cu", "selftest.cu"]
+SOURCES = ["api.cu", "preprocess.cu", "bwd_simt.cu", "fwd_simt.cu", "fwd_sm103.cu", "bwd_sm103.cu", "bwd_d256.cu",
+           "noalloc.cu", "selftest.cu"]
 
 
 def _nvcc() -> str:

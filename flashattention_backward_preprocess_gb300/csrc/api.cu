@@ -232,7 +232,8 @@ int bwd_impl(const void* dO, const void* Q, const void* K, const void* V, const 
     ws.dqacc = reinterpret_cast<float*>(static_cast<char*>(base) + L.off_dq);
     ws.dq_sem = nullptr;
     ws.dq_ticket = nullptr;
-    const bool tc = bwd_uses_tensor_cores(dtype, d);
+    const int kind = bwd_kernel_for(dtype, d);
+    const bool tc = kind == kBwdSm103;
     if (deterministic && tc) {
         ws.dq_sem = reinterpret_cast<unsigned int*>(static_cast<char*>(base) + L.off_sem);
         ws.dq_ticket = ws.dq_sem + L.sem_bytes / 4 - 1;
@@ -243,7 +244,8 @@ int bwd_impl(const void* dO, const void* Q, const void* K, const void* V, const 
         fprintf(stderr,
                 "[fa] bwd B=%d H=%d H_kv=%d S_q=%d S_k=%d d=%d causal=%d window=%d det=%d dtype=%d kernel=%s "
                 "grid=%d ws=%zu\n",
-                B, H, H_kv, S_q, S_k, d, causal, window, deterministic, dtype, tc ? "sm103" : "simt",
+                B, H, H_kv, S_q, S_k, d, causal, window, deterministic, dtype,
+                kind == kBwdSm103 ? "sm103" : (kind == kBwdD256 ? "d256" : "simt"),
                 tc ? (S_k + kTileK - 1) / kTileK * B * H_kv : 0, L.total);
     ProfRec pr;
     const bool prof = prof_begin(&pr);
@@ -253,6 +255,10 @@ int bwd_impl(const void* dO, const void* Q, const void* K, const void* V, const 
     if (prof) cudaEventRecord(pr.ev[1], st);
     if (tc) {
         e = launch_bwd_sm103(dtype, Q, K, V, dO, ws, dK, dV, s, st);
+    } else if (kind == kBwdD256) {
+        // deterministic: dK, dV on the tensor cores, dQ summed in key order on CUDA cores
+        e = launch_bwd_d256(dtype, Q, K, V, dO, ws, dK, dV, s, deterministic != 0, st);
+        if (e == cudaSuccess && deterministic) e = launch_dq_simt(dtype, Q, K, V, dO, ws, s, st);
     } else {
         // CUDA-core path: deterministic dQ comes from its own kernel, which sums each row's
         // contributions in key order; the main kernel then leaves dQ alone
@@ -331,9 +337,10 @@ int validate_bwd_args(const void* dO, const void* Q, const void* K, const void* 
 
 int set_error(int status, const char* arg, const char* reason) { return fail(status, arg, reason); }
 
-// tensor cores for f16 / bf16 at head dims up to 128; CUDA cores for f32 and d = 256
-bool bwd_uses_tensor_cores(int dtype, int d) {
-    return dtype != FA_F32 && !use_simt_for_16bit() && tc_head_dim(d) != 0;
+int bwd_kernel_for(int dtype, int d) {
+    if (dtype == FA_F32 || use_simt_for_16bit()) return kBwdSimt;
+    if (tc_head_dim(d) != 0) return kBwdSm103;
+    return d == 256 ? kBwdD256 : kBwdSimt;
 }
 
 void clear_error() { g_last_error.clear(); }

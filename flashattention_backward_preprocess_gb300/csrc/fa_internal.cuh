@@ -97,7 +97,8 @@ __host__ __device__ __forceinline__ void key_range(const Shape& s, int i0, int i
 // Head dims the library takes.  The CUDA-core kernels and the preprocess are instantiated
 // for each; the tensor-core kernels run d = 32 and 96 as d = 64 and 128 with the missing
 // columns zero-filled by TMA (their global extents and strides stay d); at d = 256 the
-// forward has a tensor-core instance of its own and the backward runs on CUDA cores.
+// forward has a tensor-core instance of its own and the backward a kernel of its own
+// (bwd_d256.cu).
 #define FA_FOR_DTYPE(dtype, DD, CALL)              \
     do {                                           \
         if ((dtype) == FA_F32) CALL(float, DD);    \
@@ -153,6 +154,10 @@ cudaError_t launch_dq_simt(int dtype, const void* Q, const void* K, const void* 
 // fwd_simt.cu
 cudaError_t launch_fwd_simt(int dtype, const void* Q, const void* K, const void* V, void* O,
                             float* LSE, const Shape& s, cudaStream_t st);
+// bwd_d256.cu (tcgen05 path for f16 / bf16 at head dim 256; skip_dq: dK, dV only)
+cudaError_t launch_bwd_d256(int dtype, const void* Q, const void* K, const void* V, const void* dO,
+                            const Workspace& ws, void* dK, void* dV, const Shape& s, bool skip_dq,
+                            cudaStream_t st);
 // bwd_sm103.cu (tcgen05 path for f16 / bf16)
 cudaError_t launch_bwd_sm103(int dtype, const void* Q, const void* K, const void* V,
                              const void* dO, const Workspace& ws, void* dK, void* dV,
@@ -170,10 +175,11 @@ int validate_bwd_args(const void* dO, const void* Q, const void* K, const void* 
                       int H_kv, int S_q, int S_k, int d, float scale, int causal, int dtype);
 int set_error(int status, const char* arg, const char* reason);
 void clear_error();
-// True when fa_bwd runs the tcgen05 kernel for this dtype and head dim (f16 / bf16 at a
-// head dim the tensor-core backward takes, unless FA_BWD_KERNEL=simt); every backward
-// entry point picks its main kernel with this one test.
-bool bwd_uses_tensor_cores(int dtype, int d);
+// The main backward kernel fa_bwd runs for a dtype and head dim; every backward entry point
+// picks it with this one function.  f16 / bf16 run a tcgen05 kernel (head dims up to 128, or
+// the d = 256 one) unless FA_BWD_KERNEL=simt; f32 runs on CUDA cores.
+enum BwdKernel { kBwdSimt = 0, kBwdSm103 = 1, kBwdD256 = 2 };
+int bwd_kernel_for(int dtype, int d);
 
 // noalloc.cu: reads the error word of the no-allocation scratch on the current device
 // into *word and clears it (0 if fa_bwd_noalloc never ran on this device).  Returns an

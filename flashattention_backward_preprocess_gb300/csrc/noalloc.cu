@@ -142,8 +142,10 @@ extern "C" int fa_bwd_noalloc(const void* dO, const void* Q, const void* K, cons
     // the preprocess pass also zeroes the dQ accumulator rows this call uses
     cudaError_t e = launch_preprocess(dtype, dO, O, LSE, ws.Dws, ws.lse2, ws.dqacc, s, S_q_pad, st);
     if (e != cudaSuccess) return set_error(FA_ERR_CUDA, "preprocess launch", cudaGetErrorString(e));
-    e = bwd_uses_tensor_cores(dtype, d) ? launch_bwd_sm103(dtype, Q, K, V, dO, ws, dK, dV, s, st)
-                                        : launch_bwd_simt(dtype, Q, K, V, dO, ws, dK, dV, s, false, st);
+    const int kind = bwd_kernel_for(dtype, d);
+    e = kind == kBwdSm103 ? launch_bwd_sm103(dtype, Q, K, V, dO, ws, dK, dV, s, st)
+        : kind == kBwdD256 ? launch_bwd_d256(dtype, Q, K, V, dO, ws, dK, dV, s, false, st)
+                           : launch_bwd_simt(dtype, Q, K, V, dO, ws, dK, dV, s, false, st);
     if (e != cudaSuccess) return set_error(FA_ERR_CUDA, "main kernel launch", cudaGetErrorString(e));
     e = launch_dq_finalize(dtype, ws.dqacc, dQ, s, st);
     if (e != cudaSuccess) return set_error(FA_ERR_CUDA, "dq finalize launch", cudaGetErrorString(e));

@@ -17,6 +17,8 @@ this library is measured on):
   bf16_b1_h32_kv8_s16384_d128_causal_w4096
                                     bf16   1 32   8   16384 16384 128   yes     1
                                     (sliding window of 4096 keys)
+  bf16_b1_h16_kv4_s4096_d256_causal bf16   1 16   4    4096  4096 256   yes     1
+  fp32_b2_h8_kv2_s2048_d128_causal  f32    2  8   2    2048  2048 128   yes     1
 
 scale = 1/sqrt(d) everywhere.
 """
@@ -100,6 +102,10 @@ WORKLOADS = {
                  seed=1239),
         Workload("bf16_b1_h32_kv8_s16384_d128_causal_w4096", "bf16", 1, 32, 8, 16384, 16384, 128, True,
                  seed=1240, window=4096),
+        # head dim 256 (the tensor-core kernel with 64-key tiles)
+        Workload("bf16_b1_h16_kv4_s4096_d256_causal", "bf16", 1, 16, 4, 4096, 4096, 256, True, seed=1241),
+        # fp32 at a size where the CUDA-core backward is measured
+        Workload("fp32_b2_h8_kv2_s2048_d128_causal", "f32", 2, 8, 2, 2048, 2048, 128, True, seed=1242),
     )
 }
 

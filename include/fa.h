@@ -76,10 +76,10 @@ typedef enum {
  *   causal        : 0 or 1
  *   dtype         : fa_dtype (F32, F16, BF16); accumulation is fp32
  *   stream        : cudaStream_t
- * F16/BF16 with d <= 128 run the tcgen05 tensor-core kernel (d = 32 and 96
- * on the d = 64 and 128 kernels, the missing columns read as zeros); F32 and
- * d = 256 (whose dK and dV alone would fill the 512 TMEM columns) run FFMA
- * kernels.
+ * F16/BF16 run tcgen05 tensor-core kernels: one for d <= 128 (d = 32 and 96
+ * on the d = 64 and 128 instances, the missing columns read as zeros), one
+ * for d = 256 (64-key tiles, dK and dV accumulated transposed); F32 runs an
+ * FFMA kernel.
  * dQ is reduced across key tiles with fp32 atomics, so dQ may differ in the
  * last bits between runs (flash_bwd.rs, "dQ must be zeroed -- backward uses
  * atomicAdd"); dK and dV are deterministic.  fa_bwd_ex(..., deterministic = 1)

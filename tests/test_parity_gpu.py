@@ -74,7 +74,9 @@ def check_full(w: Workload):
 @pytest.mark.parametrize("name", ["fp32_b1_h2_s128_d64", "bf16_b2_h8_s1024_d64_causal",
                                   "bf16_b4_h32_kv8_s2048_d128_causal", "fp16_b1_h16_s8192_d128",
                                   "bf16_b8_h16_kv2_sq512_sk4096_d64",
-                                  "bf16_b1_h32_kv8_s16384_d128_causal_w4096"])
+                                  "bf16_b1_h32_kv8_s16384_d128_causal_w4096",
+                                  "bf16_b1_h16_kv4_s4096_d256_causal",
+                                  "fp32_b2_h8_kv2_s2048_d128_causal"])
 def test_workload_full(name):
     check_full(WORKLOADS[name])
 
@@ -128,6 +130,33 @@ def test_dk_dv_deterministic_and_outputs_bounded():
         outs.append((dQ.clone(), dK.clone(), dV.clone()))
     assert torch.equal(outs[0][1], outs[1][1]) and torch.equal(outs[0][2], outs[1][2])
     assert rel_err(f64(outs[0][0]), f64(outs[1][0])) < 1e-2
+
+
+def test_accumulator_state_across_calls_and_paths():
+    """The tensor-core kernel converts dQ itself and leaves the fp32 accumulator zero; the
+    deterministic and CUDA-core paths leave it holding values and mark it, so the next
+    call's preprocess zeroes it.  A sequence of calls on one stream that switches between
+    the paths and between larger and smaller shapes must stay correct at every step."""
+    seq = [
+        ("bf16", 2, 4, 2, 640, 640, 128, True, False),   # fused
+        ("bf16", 2, 4, 2, 640, 640, 128, True, False),   # fused again: starts from its own zeroes
+        ("bf16", 1, 4, 2, 300, 300, 128, True, True),    # deterministic: leaves values
+        ("bf16", 2, 4, 2, 640, 640, 128, True, False),   # fused after it: larger than the marked part
+        ("f32", 1, 2, 1, 200, 200, 64, False, False),    # CUDA cores: leaves values
+        ("f16", 1, 2, 2, 130, 260, 64, False, False),    # fused, smaller than the marked part
+        ("bf16", 2, 4, 2, 640, 640, 128, True, False),   # fused, covers it again
+        ("bf16", 1, 2, 1, 200, 200, 256, True, False),   # d = 256 kernel: separate finalisation
+        ("bf16", 1, 4, 1, 260, 130, 64, True, False),    # fused; rows and tiles that see no key
+    ]
+    for k, (dt, B, H, H_kv, S_q, S_k, d, causal, det) in enumerate(seq):
+        w = Workload("seq", dt, B, H, H_kv, S_q, S_k, d, causal, seed=80 + k)
+        Q, K, V, dO, O, LSE = prepare(w)
+        got = fa.fa_bwd(dO, Q, K, V, O, LSE, scale=w.scale, causal=causal, deterministic=det)
+        torch.cuda.synchronize()
+        fa.fa_check_device()
+        ref = oracle.ref_bwd(f64(dO), f64(Q), f64(K), f64(V), f64(O), f64(LSE), w.scale, causal)
+        for name, g, r in zip(("dQ", "dK", "dV"), got, ref[:3]):
+            assert rel_err(f64(g), r) <= TOL[dt], (k, name, rel_err(f64(g), r))
 
 
 @pytest.mark.parametrize("dt,d,S", [("bf16", 128, 2048), ("f16", 64, 333), ("f32", 128, 77)])
@@ -309,6 +338,28 @@ def test_deterministic_dq_bench_workload_bitwise():
         assert rel_err(f64(got), r) <= TOL[w.dtype], name
 
 
+D256 = [
+    # dtype, B, H, H_kv, S_q, S_k, causal, window: the d = 256 tensor-core backward (64-key CTAs,
+    # 64-row query tiles, M = 64 products): one tile, ragged tails of both kinds, several query
+    # and key tiles with the causal diagonal inside a tile, GQA 4 and 8, S_q != S_k either way
+    # (rows that see no key), windows narrower than a tile and over several tiles
+    ("bf16", 1, 2, 2, 64, 64, False, 0),
+    ("f16", 1, 2, 1, 77, 77, True, 0),
+    ("bf16", 2, 8, 2, 700, 700, True, 0),
+    ("bf16", 1, 8, 1, 300, 513, False, 0),
+    ("f16", 1, 4, 4, 513, 300, True, 0),
+    ("bf16", 1, 4, 2, 129, 1000, True, 0),
+    ("bf16", 1, 4, 1, 600, 600, True, 50),
+    ("f16", 2, 2, 2, 400, 400, False, 150),
+]
+
+
+@pytest.mark.parametrize("case", D256, ids=lambda c: "-".join(map(str, c)))
+def test_head_dim_256_tensor_core_backward(case):
+    dt, B, H, H_kv, S_q, S_k, causal, win = case
+    check_full(Workload("d256", dt, B, H, H_kv, S_q, S_k, 256, causal, seed=91, window=win))
+
+
 HEAD_DIMS = [
     # dtype, B, H, H_kv, S_q, S_k, d, causal, window, deterministic
     ("bf16", 1, 4, 2, 300, 300, 96, True, 0, False),    # tensor cores, 128-wide kernel, 32 zero columns
@@ -316,8 +367,8 @@ HEAD_DIMS = [
     ("bf16", 1, 4, 1, 260, 260, 32, True, 0, False),    # tensor cores, 64-wide kernel
     ("f16", 2, 2, 2, 130, 390, 32, False, 100, False),  # + window
     ("bf16", 1, 4, 2, 333, 333, 96, True, 0, True),     # + deterministic dQ
-    ("bf16", 1, 2, 1, 200, 200, 256, True, 0, False),   # d = 256: tensor-core forward, CUDA-core backward
-    ("f16", 1, 2, 2, 130, 70, 256, False, 0, True),
+    ("bf16", 1, 2, 1, 200, 200, 256, True, 0, False),   # d = 256: tensor cores both ways
+    ("f16", 1, 2, 2, 130, 70, 256, False, 0, True),     # d = 256 deterministic: dQ on CUDA cores
     ("bf16", 2, 2, 1, 500, 500, 256, True, 130, False),  # + window
     ("f32", 1, 2, 1, 150, 150, 96, True, 0, False),
     ("f32", 1, 2, 2, 100, 160, 32, False, 30, True),
