@@ -170,6 +170,18 @@ def main_kernel_traffic(workload: str, deterministic: bool = False):
     return d.get("bytes_per_launch", {}).get(workload)
 
 
+FP32_SMS = 152  # GB300 streaming multiprocessors (each 128 fp32 FMA lanes)
+
+
+def main_kernel_name(w, det: bool) -> str:
+    """The main backward kernel fa_bwd runs for a workload (the library's dispatch)."""
+    if w.dtype == "f32":
+        return f"bwd_simt_kernel<f32,{w.d}>"
+    if w.d == 256:
+        return f"bwd_d256_kernel<{w.dtype}>"
+    return f"bwd_sm103_kernel<{w.dtype},{128 if w.d > 64 else 64},{'det' if det else 'default'}>"
+
+
 def workload_config(w, extra=None):
     cfg = {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.H_kv, "S_q": w.S_q, "S_k": w.S_k,
            "d": w.d, "causal": w.causal, "window": w.window, "scale": "1/sqrt(d)", "dtype": w.dtype,
@@ -361,19 +373,31 @@ def main():
     flops = w.flops()
     value = world * flops / (ms / 1e3) / 1e12
 
-    # ---- roofline of the dominant kernel (the tcgen05 main kernel)
+    # ---- roofline of the dominant kernel (the main kernel of the workload's path)
     peaks, peak_src = load_peaks()
     main_ms = ms_main / max(calls, 1)
     achieved = flops / (main_ms / 1e3) / 1e12
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    traffic = main_kernel_traffic(w.name, det)
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": traffic, "peak_source": f"{peak_src} bf16_tflops (burst)",
-                "kernel": f"bwd_sm103_kernel<{w.dtype},{w.d},{'det' if det else 'default'}>",
-                "kernel_ms": main_ms,
-                "preprocess_ms": ms_pre / max(calls, 1), "finalize_ms": ms_fin / max(calls, 1),
-                "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", 1700.0)),
-                "step_frac": (flops / (ms / 1e3) / 1e12) / peak}
+    kernel = main_kernel_name(w, det)
+    if w.dtype == "f32":
+        # CUDA-core path: FFMA peak = SMs x 128 fp32 lanes x 2 flops x the maximum SM clock
+        sm_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+        peak = FP32_SMS * 128 * 2 * sm_mhz * 1e6 / 1e12
+        roofline = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": None,
+                    "peak_source": f"{FP32_SMS} SMs x 128 fp32 FMA lanes x 2 flops x {sm_mhz:.0f} MHz "
+                                   f"({peak_src} sm_max_mhz)",
+                    "kernel": kernel, "kernel_ms": main_ms,
+                    "preprocess_ms": ms_pre / max(calls, 1), "finalize_ms": ms_fin / max(calls, 1),
+                    "step_frac": (flops / (ms / 1e3) / 1e12) / peak}
+    else:
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        traffic = main_kernel_traffic(w.name, det)
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": traffic, "peak_source": f"{peak_src} bf16_tflops (burst)",
+                    "kernel": kernel, "kernel_ms": main_ms,
+                    "preprocess_ms": ms_pre / max(calls, 1), "finalize_ms": ms_fin / max(calls, 1),
+                    "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", 1700.0)),
+                    "step_frac": (flops / (ms / 1e3) / 1e12) / peak}
 
     # ---- end to end through the host-buffer entry point (no sliding window or
     # deterministic mode there)

@@ -337,6 +337,32 @@ int validate_bwd_args(const void* dO, const void* Q, const void* K, const void* 
 
 int set_error(int status, const char* arg, const char* reason) { return fail(status, arg, reason); }
 
+int key_tile_split(const Shape& s, int bn, int bm) {
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+            sms = 148;
+    }
+    const int n_key_tiles = (s.S_k + bn - 1) / bn;
+    const long groups = (long)s.B * s.H_kv;
+    const int g = s.H / s.H_kv;
+    long total = 0, most = 0;
+    for (int kt = 0; kt < n_key_tiles; ++kt) {
+        int lo, hi;
+        query_range(s, kt * bn, kt * bn + bn < s.S_k ? kt * bn + bn : s.S_k, lo, hi);
+        const long its = hi > lo ? (long)g * ((hi + bm - 1) / bm - lo / bm) : 0;
+        total += its * groups;
+        most = its > most ? its : most;
+    }
+    // a grid of fewer CTAs than SMs is not split: clusters of two CTAs that each fill an SM
+    // fit about 72 pairs at a time, so the halves ran in two waves (measured: the causal
+    // S = 1024, d = 64 workload went from 24 to 33 us)
+    if ((long)n_key_tiles * groups < sms) return 1;
+    return (double)most > 1.05 * (double)total / sms ? 2 : 1;
+}
+
 int bwd_kernel_for(int dtype, int d) {
     if (dtype == FA_F32 || use_simt_for_16bit()) return kBwdSimt;
     if (tc_head_dim(d) != 0) return kBwdSm103;

@@ -18,11 +18,15 @@
 //     128-column halves that share one TMEM buffer;
 //   * the softmax-gradient warps write P and dS to shared memory, 16-bit, as the B operand
 //     of the dV^T / dK^T products and (dS) the A operand of the dQ product;
-//   * TMA stages K, V once and Q, dO (64 rows, 32 KB each) through a 2-stage ring; the dQ
-//     halves are drained TMEM -> registers -> shared memory (the iteration's dO tile, free
-//     once the dV^T product ran, then its Q tile, free once the dK^T product ran) -> TMA
-//     bulk reduce-add into the fp32 accumulator, which also frees the stage for the load
-//     two iterations ahead.
+//   * TMA stages K, V once and Q, dO (64 rows, 32 KB each) through a 2-stage ring; a stage
+//     is free for the load two iterations ahead as soon as the dK^T product, the last one
+//     reading it, is done;
+//   * the dQ halves are drained TMEM -> registers -> fp32 vector reductions
+//     (red.global.add.v2.f32, all 32 lanes of each drain warp) into the accumulator.  dQ is
+//     not staged through shared memory for bulk reduce-adds as it is at d <= 128: that
+//     holds the stage until TMA has read it, and the products (~270 KB of shared-memory
+//     operands per iteration) compete with the staging traffic; measured 36 % slower.
+//     The reductions bound the kernel: 64 KB of fp32 adds per 10.5 MFLOP iteration.
 // TMEM (512 columns): dV^T [0, 128), dK^T [128, 256), S [256, 320), dP [320, 384), dQ half
 // [384, 512).  Shared memory: K, V 32 KB each, 2 x (Q 32 KB + dO 32 KB), P and dS tiles
 // 2 x 8 KB each, LSE / D rows: 230 KB.
@@ -48,7 +52,6 @@ constexpr int kThreads = 14 * 32;
 constexpr int kWarpDrain0 = 0, kWarpSoft0 = 4, kNumSoftWarps = 8, kWarpTma = 12, kWarpMma = 13;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TM_DV = 0, TM_DK = 128, TM_S = 256, TM_DP = 320, TM_DQ = 384;
-constexpr uint32_t kDrainBarrier = 1;  // named barrier of the 4 drain warps
 
 constexpr uint32_t kBox = 64 * 128;                 // one 64-column box of a 64-row tile (8 KB)
 constexpr uint32_t kTile = 4 * kBox;                // a 64 x 256 16-bit tile (32 KB)
@@ -74,7 +77,7 @@ enum {
     B_DQ_EMPTY,  // that half read out of TMEM (4 drain warps)
     B_PT_FREE,   // P tile k no longer read (MMA commit after the dV^T product); 2 slots
     B_DT_FREE = B_PT_FREE + 2,  // dS tile k no longer read (commit after the dQ products); 2 slots
-    B_ACC = B_DT_FREE + 2,      // every product done (MMA commit)
+    B_ACC = B_DT_FREE + 2,       // every product done (MMA commit)
     B_FINAL,     // MMA shutdown
     B_STAGE0     // STAGES "full" barriers, then STAGES "empty" barriers
 };
@@ -88,12 +91,14 @@ struct Params {
     const float* Dws;
     void* dK;
     void* dV;
+    float* dqacc;  // fp32 dQ accumulator [B*H][S_q][256]
     unsigned int* err;
     int B, H, H_kv, S_q, S_k, S_q_pad;
     float scale, scale_log2;
     int causal, window;
     int group_chunk;  // (b, kv head) groups per block of the CTA order (divides B * H_kv)
     int skip_dq;      // 1: leave dQ alone (deterministic mode computes it in a kernel of its own)
+    int split;        // CTAs per key tile (1, or 2 = a cluster splitting the query tiles, see below)
 };
 
 template <bool kBF16>
@@ -119,6 +124,26 @@ __device__ __forceinline__ void tmem_ld16x256_x4(uint32_t taddr, uint32_t (&r)[1
         : "r"(taddr));
 }
 
+// 16 TMEM lanes x 128 columns: register 4j + 0/1 of thread t holds row t/4, columns
+// 8j + 2(t%4) + 0/1; registers 4j + 2/3 row t/4 + 8 (j = 0..15).
+__device__ __forceinline__ void tmem_ld16x256_x16(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+        "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr));
+}
+
 // Byte offset of element (row, col) of a 128-byte-swizzled tile with 128-byte rows
 // (64 16-bit or 32 fp32 columns): 8-row atoms of 1024 bytes, 16-byte chunks XOR row % 8.
 __device__ __forceinline__ uint32_t sw128_off(int row, int byte_in_row) {
@@ -126,11 +151,27 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int byte_in_row) {
                       (byte_in_row & 15));
 }
 
+// dV and scale * dK for keys j0 .. j0 + 31 (those below S_k) at head-dim index dcol
+template <typename T>
+__device__ __forceinline__ void write_dkv(const Params& p, int bkv, int j0, int dcol, const uint32_t (&rv)[32],
+                                          const uint32_t (&rk)[32]) {
+    T* dVb = static_cast<T*>(p.dV) + (size_t)bkv * p.S_k * D + dcol;
+    T* dKb = static_cast<T*>(p.dK) + (size_t)bkv * p.S_k * D + dcol;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        const int j = j0 + k;
+        if (j < p.S_k) {
+            dVb[(size_t)j * D] = TypeTraits<T>::from_f32(__uint_as_float(rv[k]));
+            dKb[(size_t)j * D] = TypeTraits<T>::from_f32(__uint_as_float(rk[k]) * p.scale);
+        }
+    }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                    const __grid_constant__ CUtensorMap tmdQ, const Params p) {
+                    const Params p) {
     constexpr bool kBF16 = TypeTraits<T>::kId == FA_BF16;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = ptx::smem_u32(smem);
@@ -141,12 +182,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar_full = [&](int s) { return bar(B_STAGE0 + s); };
     auto bar_empty = [&](int s) { return bar(B_STAGE0 + STAGES + s); };
 
-    // ---- work assignment (as the d <= 128 kernel): blockIdx.x = (block of group_chunk
-    // (b, kv head) groups) x key tile x (group within the block); each CTA walks its query
-    // tiles from the last one down, the group's heads innermost.
+    // ---- work assignment (as the d <= 128 kernel): item = (block of group_chunk (b, kv head)
+    // groups) x key tile x (group within the block); each CTA walks its query tiles from the
+    // last one down, the group's heads innermost.  With split = 2 the two CTAs of a cluster
+    // share one item, each taking one contiguous half of its query tiles (a long causal key
+    // tile would otherwise set the kernel's time alone), and add their dK / dV partials
+    // through distributed shared memory at the end.
     const int n_key_tiles = (p.S_k + BN - 1) / BN;
-    const int chunk = blockIdx.x / (n_key_tiles * p.group_chunk);
-    const int in_chunk = blockIdx.x % (n_key_tiles * p.group_chunk);
+    const int rank = (int)(blockIdx.x % (unsigned)p.split);  // rank within the cluster (1-D)
+    const int item = (int)(blockIdx.x / (unsigned)p.split);
+    const int chunk = item / (n_key_tiles * p.group_chunk);
+    const int in_chunk = item % (n_key_tiles * p.group_chunk);
     const int n_tile = in_chunk / p.group_chunk;
     const int bkv = chunk * p.group_chunk + in_chunk % p.group_chunk;
     const int b = bkv / p.H_kv, hk = bkv % p.H_kv;
@@ -160,8 +206,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     sh.window = p.window;
     int q_lo, q_hi;
     query_range(sh, n0, min(n0 + BN, p.S_k), q_lo, q_hi);
-    const int m_start = q_lo / BM;
-    const int m_end = q_hi > q_lo ? (q_hi + BM - 1) / BM : m_start;
+    const int m_first = q_lo / BM;
+    const int m_last = q_hi > q_lo ? (q_hi + BM - 1) / BM : m_first;
+    // this CTA's query tiles [m_start, m_end)
+    const int m_start = m_first + (m_last - m_first) * rank / p.split;
+    const int m_end = m_first + (m_last - m_first) * (rank + 1) / p.split;
     const int n_it = g * (m_end - m_start);
     auto iter_coords = [&](int it, int& bh, int& m0) {
         m0 = (m_end - 1 - it / g) * BM;
@@ -197,10 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tma_load_3d(sbase + OFF_K + x * kBox, &tmK, x * 64, n0, bkv, bar(B_KV));
                 ptx::tma_load_3d(sbase + OFF_V + x * kBox, &tmV, x * 64, n0, bkv, bar(B_KV));
             }
-            int issued = 0;
-            for (int it = 0; it < n_it; ++it) {
+            auto load_stage = [&](int it) {
                 const int s = it % STAGES;
-                if (it >= STAGES && !wait_bar(bar_empty(s), ((it / STAGES) - 1) & 1, abort_flag, p.err)) break;
                 int bh, m0;
                 iter_coords(it, bh, m0);
                 ptx::mbar_arrive_expect_tx(bar_full(s), 2 * kTile + 2 * BM * 4);
@@ -211,6 +258,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const size_t row0 = (size_t)bh * p.S_q_pad + m0;
                 ptx::bulk_load(sbase + OFF_LSE + s * BM * 4, p.lse2 + row0, BM * 4, bar_full(s));
                 ptx::bulk_load(sbase + OFF_DD + s * BM * 4, p.Dws + row0, BM * 4, bar_full(s));
+            };
+            int issued = 0;
+            for (int it = 0; it < n_it; ++it) {
+                const int s = it % STAGES;
+                // stage s was last read by the dK^T product of iteration it - 2 (MMA commit)
+                if (it >= STAGES && !wait_bar(bar_empty(s), ((it / STAGES) - 1) & 1, abort_flag, p.err)) break;
+                load_stage(it);
                 issued = it + 1;
             }
             // never leave copies in flight into shared memory that is about to be released
@@ -283,6 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = wait_bar(bar(B_DS_READY), it & 1, abort_flag, p.err))) break;
                 ptx::tc_fence_after();
                 gemm_t(tmem + TM_DK, sQ, sdS, it > 0);
+                ptx::mma_commit(bar_empty(s));  // Q(i), dO(i) read for the last time
                 if (!p.skip_dq) {
                     // dQ low half into the dQ buffer once the drain read the previous high half
                     if (it > 0 && !(ok = wait_bar(bar(B_DQ_EMPTY), 1, abort_flag, p.err))) break;
@@ -300,8 +355,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tc_fence_after();
                     gemm_q(sdS, 1);
                     ptx::mma_commit(bar(B_DQ_FULL));
-                } else {
-                    ptx::mma_commit(bar_empty(s));  // Q(i), dO(i) read for the last time
                 }
                 ptx::mma_commit(bar(B_DT_FREE + (it & 1)));
             }
@@ -394,14 +447,75 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(B_DS_READY));
         }
-        // ---- epilogue: dV^T and scale * dK^T rows (one head-dim index per thread) to dV, dK
+        // ---- epilogue: dV^T and scale * dK^T rows (one head-dim index per thread) to dV, dK.
+        // In a split pair the rows are written after the CTA barrier at the end instead.
         if (ok && n_it > 0) ok = wait_bar_warp(bar(B_ACC), 0, abort_flag, p.err);
-        if (ok) {
+        if (ok && p.split == 1) {
             ptx::tc_fence_after();
             const int dcol = 128 * hc + 32 * qd + lane;  // head-dim index of this thread
-            T* dVb = static_cast<T*>(p.dV) + (size_t)bkv * p.S_k * D + dcol;
-            T* dKb = static_cast<T*>(p.dK) + (size_t)bkv * p.S_k * D + dcol;
 #pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t rv[32], rk[32];
+                if (n_it > 0) {
+                    ptx::tmem_ld32p(tmem + TM_DV + 64 * hc + lane_base + 32 * c, rv);
+                    ptx::tmem_ld32p(tmem + TM_DK + 64 * hc + lane_base + 32 * c, rk);
+                    ptx::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) rv[k] = rk[k] = 0u;
+                }
+                write_dkv<T>(p, bkv, n0 + 32 * c, dcol, rv, rk);
+            }
+        }
+    } else if (warp >= kWarpDrain0 && warp < kWarpDrain0 + 4) {
+        // ------------------------------------------------------------ dQ drain
+        // Warp qd reads the 16 query rows of its lane quadrant, a whole 128-column half at a
+        // time, with all 32 threads (rows t/4 and t/4 + 8, column pairs), releases the TMEM
+        // buffer, then adds the values into the accumulator rows with fp32 vector reductions.
+        const int qd = warp;
+        const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+        const int ra = 16 * qd + (lane >> 2), rb = ra + 8;
+        const int c0 = 2 * (lane & 3);
+        bool ok = !*abort_flag && !p.skip_dq;
+        for (int it = 0; ok && it < n_it; ++it) {
+            int bh, m0;
+            iter_coords(it, bh, m0);
+            const bool a_ok = m0 + ra < p.S_q, b_ok = m0 + rb < p.S_q;
+            float* ga = p.dqacc + ((size_t)bh * p.S_q + m0 + ra) * D + c0;
+            float* gb = ga + 8 * D;
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                if (!(ok = wait_bar_warp(bar(B_DQ_FULL), h, abort_flag, p.err))) break;
+                ptx::tc_fence_after();
+                uint32_t r[64];
+                tmem_ld16x256_x16(tmem + TM_DQ + lane_base, r);
+                ptx::tmem_wait_ld();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(B_DQ_EMPTY));
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int col = 128 * h + 8 * j;
+                    if (a_ok) ptx::red_add_v2(ga + col, __uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]));
+                    if (b_ok) ptx::red_add_v2(gb + col, __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                }
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (p.split > 1) {
+        // Rank 1 parks its fp32 dK / dV partial sums in its shared memory (fp32, [key][d], over
+        // the Q and dO stages, whose loads have all landed and been read) after the barrier
+        // above; rank 0 adds them after the cluster barrier.
+        if (rank == 1 && warp >= kWarpSoft0 && warp < kWarpSoft0 + kNumSoftWarps && !*abort_flag) {
+            const int qd = warp & 3, hc = (warp - kWarpSoft0) >> 2;
+            const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+            const int dcol = 128 * hc + 32 * qd + lane;
+            float* park = reinterpret_cast<float*>(smem + OFF_Q);  // dV part, then dK part
+#pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t rv[32], rk[32];
                 if (n_it > 0) {
@@ -414,100 +528,61 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
 #pragma unroll
                 for (int k = 0; k < 32; ++k) {
-                    const int j = n0 + 32 * c + k;
-                    if (j < p.S_k) {
-                        dVb[(size_t)j * D] = TypeTraits<T>::from_f32(__uint_as_float(rv[k]));
-                        dKb[(size_t)j * D] = TypeTraits<T>::from_f32(__uint_as_float(rk[k]) * p.scale);
-                    }
+                    park[(32 * c + k) * D + dcol] = __uint_as_float(rv[k]);
+                    park[BN * D + (32 * c + k) * D + dcol] = __uint_as_float(rk[k]);
                 }
             }
         }
-    } else if (warp >= kWarpDrain0 && warp < kWarpDrain0 + 4) {
-        // ------------------------------------------------------------ dQ drain
-        // Thread t < 16 of warp qd owns query row 16 qd + t (TMEM lane 32 qd + t).  Each half
-        // (128 fp32 columns) goes TMEM -> registers (64 columns at a time) -> four 64 x 32 fp32
-        // boxes in shared memory (128-byte swizzle) -> TMA reduce-add.  The low half is staged
-        // in the iteration's dO tile (the dV^T product, committed before it, no longer reads
-        // it), the high half in its Q tile (likewise the dK^T product); once both reduces have
-        // read their boxes the stage is free for the load two iterations ahead.
-        const int qd = warp;
-        const int t = threadIdx.x;  // 0..127
-        const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
-        const int row = 16 * qd + lane;
-        bool ok = !*abort_flag && !p.skip_dq;
-        for (int it = 0; ok && it < n_it; ++it) {
-            const int s = it % STAGES;
-            int bh, m0;
-            iter_coords(it, bh, m0);
+        // every thread of both CTAs: rank 1's partial sums are in its shared memory
+        ptx::cluster_sync();
+        if (rank == 0 && warp >= kWarpSoft0 && warp < kWarpSoft0 + kNumSoftWarps && !*abort_flag) {
+            const int qd = warp & 3, hc = (warp - kWarpSoft0) >> 2;
+            const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+            const int dcol = 128 * hc + 32 * qd + lane;
+            const uint32_t park = ptx::mapa_shared(sbase + OFF_Q, 1);
 #pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                ok = ptx::named_bar_and(kDrainBarrier, 128, wait_bar(bar(B_DQ_FULL), h, abort_flag, p.err));
-                if (!ok) break;
-                ptx::tc_fence_after();
-                uint8_t* area = smem + (h == 0 ? OFF_DO : OFF_Q) + s * kTile;
-#pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2) {  // 64 columns at a time
-                    uint32_t rr[64];
-                    ptx::tmem_ld32p(tmem + TM_DQ + lane_base + 64 * q2, rr);
-                    ptx::tmem_ld32p(tmem + TM_DQ + lane_base + 64 * q2 + 32, rr + 32);
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t rv[32], rk[32];
+                if (n_it > 0) {
+                    ptx::tmem_ld32p(tmem + TM_DV + 64 * hc + lane_base + 32 * c, rv);
+                    ptx::tmem_ld32p(tmem + TM_DK + 64 * hc + lane_base + 32 * c, rk);
                     ptx::tmem_wait_ld();
-                    if (q2 == 1) {
-                        ptx::tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive(bar(B_DQ_EMPTY));
-                    }
-                    if (lane < 16) {
+                } else {
 #pragma unroll
-                        for (int bx = 0; bx < 2; ++bx)
-#pragma unroll
-                            for (int cq = 0; cq < 8; ++cq) {
-                                const int e = bx * 32 + cq * 4;
-                                *reinterpret_cast<uint4*>(area + (2 * q2 + bx) * kBox + sw128_off(row, cq * 16)) =
-                                    make_uint4(rr[e], rr[e + 1], rr[e + 2], rr[e + 3]);
-                            }
-                    }
+                    for (int k = 0; k < 32; ++k) rv[k] = rk[k] = 0u;
                 }
-                ptx::fence_proxy_async_smem();  // the staged dQ before the bulk reads
-                ptx::named_bar_sync(kDrainBarrier, 128);
-                if (t == 0) {
-                    const uint64_t pol = ptx::policy_evict_last();
 #pragma unroll
-                    for (int bx = 0; bx < 4; ++bx)
-                        ptx::tma_reduce_add_3d_hint(&tmdQ, ptx::smem_u32(area + bx * kBox), 128 * h + 32 * bx, m0, bh,
-                                                    pol);
-                    ptx::bulk_commit_group();
-                    if (h == 1) {
-                        ptx::bulk_wait_read_all();  // both halves read: the stage is free
-                        ptx::mbar_arrive(bar_empty(s));
-                    }
+                for (int k = 0; k < 32; ++k) {
+                    const uint32_t o = (uint32_t)(((32 * c + k) * D + dcol) * 4);
+                    rv[k] = __float_as_uint(__uint_as_float(rv[k]) + ptx::ld_shared_cluster_f32(park + o));
+                    rk[k] = __float_as_uint(__uint_as_float(rk[k]) + ptx::ld_shared_cluster_f32(park + BN * D * 4 + o));
                 }
+                write_dkv<T>(p, bkv, n0 + 32 * c, dcol, rv, rk);
             }
         }
-        if (t == 0) ptx::bulk_wait_all();
+        ptx::tc_fence_before();
+        ptx::cluster_sync();  // rank 0 has read rank 1's shared memory: both may exit
+        ptx::tc_fence_after();
     }
-
-    ptx::tc_fence_before();
-    __syncthreads();
-    ptx::tc_fence_after();
     if (warp == kWarpMma) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
 template <typename T>
 cudaError_t launch_t(const void* Q, const void* K, const void* V, const void* dO, const Workspace& ws, void* dK,
                      void* dV, const Shape& s, bool skip_dq, cudaStream_t st) {
-    CUtensorMap tq, tk, tv, tdo, tdq;
+    CUtensorMap tq, tk, tv, tdo;
     const CUtensorMapDataType dt =
         TypeTraits<T>::kId == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     if (s.d != D || !tma_map_3d(&tq, Q, dt, 2, s.B * s.H, s.S_q, D, BM) ||
         !tma_map_3d(&tk, K, dt, 2, s.B * s.H_kv, s.S_k, D, BN) || !tma_map_3d(&tv, V, dt, 2, s.B * s.H_kv, s.S_k, D, BN) ||
-        !tma_map_3d(&tdo, dO, dt, 2, s.B * s.H, s.S_q, D, BM) ||
-        !tma_map_3d(&tdq, ws.dqacc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s.B * s.H, s.S_q, D, BM))
+        !tma_map_3d(&tdo, dO, dt, 2, s.B * s.H, s.S_q, D, BM))
         return cudaErrorInvalidValue;
     Params p;
     p.lse2 = ws.lse2;
     p.Dws = ws.Dws;
     p.dK = dK;
     p.dV = dV;
+    p.dqacc = ws.dqacc;
     p.err = ws.err;
     p.B = s.B;
     p.H = s.H;
@@ -527,9 +602,25 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, const void* dO
     if (!s.causal || s.window > 0) p.group_chunk = groups % 4 == 0 ? 4 : (groups % 2 == 0 ? 2 : groups);
     cudaError_t e = cudaFuncSetAttribute(bwd_d256_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
     if (e != cudaSuccess) return e;
-    const long grid = (long)((s.S_k + BN - 1) / BN) * s.B * s.H_kv;
-    bwd_d256_kernel<T><<<(unsigned)grid, kThreads, SMEM, st>>>(tq, tk, tv, tdo, tdq, p);
-    return cudaGetLastError();
+    p.split = key_tile_split(s, BN, BM);
+    const long grid = (long)((s.S_k + BN - 1) / BN) * s.B * s.H_kv * p.split;
+    if (p.split == 1) {
+        bwd_d256_kernel<T><<<(unsigned)grid, kThreads, SMEM, st>>>(tq, tk, tv, tdo, p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, bwd_d256_kernel<T>, tq, tk, tv, tdo, p);
 }
 
 }  // namespace

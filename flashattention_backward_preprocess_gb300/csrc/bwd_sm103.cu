@@ -161,7 +161,7 @@ __device__ __forceinline__ float2 unpack2(uint32_t v) {
 
 static_assert(B_STAGE0 == 23, "Cfg::kNumBars counts 23 named barriers before the stage ring");
 
-template <typename T, int D, bool kDet>
+template <typename T, int D, bool kDet, int kSplit>
 __global__ void __launch_bounds__(threads_for(kDet, D), 1)
     bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -215,7 +215,11 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
     // running side by side reduce into and read the same dQ / Q / dO tiles at about the
     // same time.  Within a group a lower key tile always has a lower logical index.
     const int n_key_tiles = (p.S_k + BN - 1) / BN;
-    const int blk = kDet ? (int)*ticket_slot : (int)blockIdx.x;
+    // With split = 2 (default mode only) the two CTAs of a cluster share one logical index,
+    // each taking one contiguous half of its query tiles, and add their dK / dV partials
+    // through distributed shared memory at the end (small grids, long causal key tiles).
+    const int rank = kSplit > 1 ? (int)(blockIdx.x % kSplit) : 0;  // rank within the 1-D cluster
+    const int blk = kDet ? (int)*ticket_slot : (int)(blockIdx.x / kSplit);
     const int chunk = blk / (n_key_tiles * p.group_chunk);
     const int in_chunk = blk % (n_key_tiles * p.group_chunk);
     const int n_tile = in_chunk / p.group_chunk;
@@ -234,8 +238,11 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
     int q_lo, q_hi;
     query_range(sh, n0, min(n0 + BN, p.S_k), q_lo, q_hi);
     const int m_tiles = (p.S_q + BM - 1) / BM;
-    const int m_start = q_lo / BM;
-    const int m_end = q_hi > q_lo ? (q_hi + BM - 1) / BM : m_start;
+    const int m_first = q_lo / BM;
+    const int m_last = q_hi > q_lo ? (q_hi + BM - 1) / BM : m_first;
+    // this CTA's query tiles [m_start, m_end)
+    const int m_start = kSplit > 1 ? m_first + (m_last - m_first) * rank / kSplit : m_first;
+    const int m_end = kSplit > 1 ? m_first + (m_last - m_first) * (rank + 1) / kSplit : m_last;
     const int nm = m_end - m_start;
     const int n_it = g * nm;
 
@@ -563,9 +570,10 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(B_DS_READY));
         }
-        // ---- epilogue: dV and scale * dK rows to global, columns [hf*D/2, hf*D/2 + D/2)
+        // ---- epilogue: dV and scale * dK rows to global, columns [hf*D/2, hf*D/2 + D/2).  In a
+        // split pair the rows are written after the CTA barrier at the end instead (below).
         if (ok && n_it > 0) ok = wait_bar_warp(bar(B_ACC), 0, abort_flag, p.err);
-        if (ok) {
+        if (ok && kSplit == 1) {
             ptx::tc_fence_after();
             T* dVrow = static_cast<T*>(p.dV) + ((size_t)bkv * p.S_k + j) * p.d;
             T* dKrow = static_cast<T*>(p.dK) + ((size_t)bkv * p.S_k + j) * p.d;
@@ -710,6 +718,87 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
+    if (kSplit > 1) {
+        // Rank 1 parks its fp32 dK / dV partial sums in its shared memory (over the Q / dO / dS
+        // tiles, rows padded by four words): only after the barrier above, which the drain's
+        // issuing thread reaches once its bulk reduce-adds (which read the dS and dO tiles)
+        // are complete.  Rank 0 adds them after the cluster barrier.
+        if (rank == 1 && warp >= kWarpSoft0 && warp < kWarpSoft0 + kNumSoftWarps && !*abort_flag) {
+            const int qd = warp & 3, hf = (warp - kWarpSoft0) >> 2;
+            const int t = qd * 32 + lane;
+            const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+            ptx::tc_fence_after();
+            float* park = reinterpret_cast<float*>(smem + C::OFF_Q);  // dV part, then dK part
+#pragma unroll
+            for (int cc = 0; cc < D / 64; ++cc) {
+                const int c = hf * (D / 64) + cc;  // 32-column chunk
+                uint32_t rv[32], rk[32];
+                if (n_it > 0) {
+                    ptx::tmem_ld32p(tmem + C::TM_DV + lane_off + c * 32, rv);
+                    ptx::tmem_ld32p(tmem + C::TM_DK + lane_off + c * 32, rk);
+                    ptx::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) rv[k] = rk[k] = 0u;
+                }
+#pragma unroll
+                for (int k = 0; k < 32; k += 4) {
+                    *reinterpret_cast<uint4*>(park + t * (D + 4) + c * 32 + k) =
+                        make_uint4(rv[k], rv[k + 1], rv[k + 2], rv[k + 3]);
+                    *reinterpret_cast<uint4*>(park + BN * (D + 4) + t * (D + 4) + c * 32 + k) =
+                        make_uint4(rk[k], rk[k + 1], rk[k + 2], rk[k + 3]);
+                }
+            }
+        }
+        // every thread of both CTAs: rank 1's partial sums are in its shared memory
+        ptx::cluster_sync();
+        if (rank == 0 && warp >= kWarpSoft0 && warp < kWarpSoft0 + kNumSoftWarps && !*abort_flag) {
+            const int qd = warp & 3, hf = (warp - kWarpSoft0) >> 2;
+            const int t = qd * 32 + lane;
+            const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+            const int j = n0 + t;
+            const uint32_t park = ptx::mapa_shared(sbase + C::OFF_Q, 1);
+            T* dVrow = static_cast<T*>(p.dV) + ((size_t)bkv * p.S_k + j) * p.d;
+            T* dKrow = static_cast<T*>(p.dK) + ((size_t)bkv * p.S_k + j) * p.d;
+#pragma unroll 1
+            for (int cc = 0; cc < D / 64; ++cc) {
+                const int c = hf * (D / 64) + cc;
+                uint32_t rv[32], rk[32];
+                if (n_it > 0) {
+                    ptx::tmem_ld32p(tmem + C::TM_DV + lane_off + c * 32, rv);
+                    ptx::tmem_ld32p(tmem + C::TM_DK + lane_off + c * 32, rk);
+                    ptx::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) rv[k] = rk[k] = 0u;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    uint32_t ov[4], ok4[4];
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const uint32_t o = (uint32_t)((t * (D + 4) + c * 32 + u * 8 + 4 * h2) * 4);
+                        const float4 pv = ptx::ld_shared_cluster_v4(park + o);
+                        const float4 pk = ptx::ld_shared_cluster_v4(park + BN * (D + 4) * 4 + o);
+                        const int e = u * 8 + 4 * h2;
+                        ov[2 * h2] = pack2<kBF16>(__uint_as_float(rv[e]) + pv.x, __uint_as_float(rv[e + 1]) + pv.y);
+                        ov[2 * h2 + 1] = pack2<kBF16>(__uint_as_float(rv[e + 2]) + pv.z, __uint_as_float(rv[e + 3]) + pv.w);
+                        ok4[2 * h2] = pack2<kBF16>((__uint_as_float(rk[e]) + pk.x) * p.scale,
+                                                   (__uint_as_float(rk[e + 1]) + pk.y) * p.scale);
+                        ok4[2 * h2 + 1] = pack2<kBF16>((__uint_as_float(rk[e + 2]) + pk.z) * p.scale,
+                                                       (__uint_as_float(rk[e + 3]) + pk.w) * p.scale);
+                    }
+                    if (j < p.S_k && c * 32 + u * 8 < p.d) {
+                        *reinterpret_cast<uint4*>(dVrow + c * 32 + u * 8) = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+                        *reinterpret_cast<uint4*>(dKrow + c * 32 + u * 8) = make_uint4(ok4[0], ok4[1], ok4[2], ok4[3]);
+                    }
+                }
+            }
+        }
+        ptx::tc_fence_before();
+        ptx::cluster_sync();  // rank 0 has read rank 1's shared memory: both may exit
+        ptx::tc_fence_after();
+    }
     if (warp == kWarpMma) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -793,12 +882,33 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, const void* dO
     p.group_chunk = groups;
     if ((!s.causal || s.window > 0) && ws.dq_sem == nullptr)
         p.group_chunk = groups % 4 == 0 ? 4 : (groups % 2 == 0 ? 2 : groups);
-    auto kern = ws.dq_sem != nullptr ? bwd_sm103_kernel<T, D, true> : bwd_sm103_kernel<T, D, false>;
+    // a cluster of two CTAs per key tile for small grids and long causal key tiles (the
+    // deterministic mode takes its CTA indices from a start-order ticket, which cannot pair
+    // cluster ranks: one CTA per key tile there)
+    const int split = ws.dq_sem != nullptr ? 1 : key_tile_split(s, BN, BM);
+    auto kern = ws.dq_sem != nullptr ? bwd_sm103_kernel<T, D, true, 1>
+                                     : (split == 2 ? bwd_sm103_kernel<T, D, false, 2> : bwd_sm103_kernel<T, D, false, 1>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
-    const long grid = (long)((s.S_k + BN - 1) / BN) * s.B * s.H_kv;
-    kern<<<(unsigned)grid, threads_for(ws.dq_sem != nullptr, D), C::SMEM, st>>>(tq, tk, tv, tdo, tdq, p);
-    return cudaGetLastError();
+    const long grid = (long)((s.S_k + BN - 1) / BN) * s.B * s.H_kv * split;
+    const int threads = threads_for(ws.dq_sem != nullptr, D);
+    if (split == 1) {
+        kern<<<(unsigned)grid, threads, C::SMEM, st>>>(tq, tk, tv, tdo, tdq, p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, tdo, tdq, p);
 }
 
 }  // namespace

@@ -169,6 +169,12 @@ cudaError_t launch_fwd_sm103(int dtype, const void* Q, const void* K, const void
 // selftest.cu
 cudaError_t launch_wait_selftest(unsigned int* err, uint64_t limit_ns, cudaStream_t st);
 
+// api.cu: CTAs per key tile for a tensor-core backward launch with bn-key CTAs walking
+// bm-row query tiles: 2 (a cluster that splits each key tile's query tiles in halves) when
+// the CTA with the most iterations would outlast an even share of the whole over the SMs
+// (long causal problems), else 1.
+int key_tile_split(const Shape& s, int bn, int bm);
+
 // api.cu: argument checks and error text shared by the entry points.
 int validate_bwd_args(const void* dO, const void* Q, const void* K, const void* V, const void* O,
                       const float* LSE, const void* dQ, const void* dK, const void* dV, int B, int H,

@@ -56,8 +56,9 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const T* __restrict__ d
 #pragma unroll
         for (int ch = lane_in_row; ch < CPR; ch += LPR) {
             const size_t off = ((size_t)bh * S_q + i) * D + (size_t)ch * VEC;
-            const int4 a = __ldg(reinterpret_cast<const int4*>(dO + off));
-            const int4 b = __ldg(reinterpret_cast<const int4*>(O + off));
+            // streaming loads (evict first): dO and O are read once here
+            const int4 a = __ldcs(reinterpret_cast<const int4*>(dO + off));
+            const int4 b = __ldcs(reinterpret_cast<const int4*>(O + off));
             const T* ta = reinterpret_cast<const T*>(&a);
             const T* tb = reinterpret_cast<const T*>(&b);
 #pragma unroll
@@ -90,8 +91,10 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const float* __restric
     // n8 = number of 8-element groups; d is a multiple of 8 so rows never split.
     for (size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x; g < n8;
          g += (size_t)gridDim.x * blockDim.x) {
-        const float4 a = __ldg(reinterpret_cast<const float4*>(acc) + 2 * g);
-        const float4 b = __ldg(reinterpret_cast<const float4*>(acc) + 2 * g + 1);
+        // streaming loads and stores (evict first): the lines of the accumulator the main
+        // kernel's reduce-adds left in L2 are not pushed out by the ones read from DRAM
+        const float4 a = __ldcs(reinterpret_cast<const float4*>(acc) + 2 * g);
+        const float4 b = __ldcs(reinterpret_cast<const float4*>(acc) + 2 * g + 1);
         const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
         if constexpr (sizeof(T) == 4) {
             float4* o = reinterpret_cast<float4*>(dQ) + 2 * g;
@@ -101,7 +104,7 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const float* __restric
             alignas(16) T t[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) t[k] = TypeTraits<T>::from_f32(v[k] * scale);
-            reinterpret_cast<int4*>(dQ)[g] = *reinterpret_cast<const int4*>(t);
+            __stcs(reinterpret_cast<int4*>(dQ) + g, *reinterpret_cast<const int4*>(t));
         }
     }
 }
