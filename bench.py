@@ -143,17 +143,25 @@ def max_over_ranks(x: float, world: int, device) -> float:
     return float(t.item())
 
 
-def kernel_source_hash() -> str:
-    """Hash of the main kernel's sources: ncu traffic counters are only valid for this exact kernel."""
+# Sources each main kernel is built from: ncu traffic counters are only valid for this exact code.
+KERNEL_SOURCES = {
+    "bwd_sm103_kernel": ("bwd_sm103.cu", "sm103_ptx.cuh", "bounded_wait.cuh", "fa_internal.cuh"),
+    "bwd_d256_kernel": ("bwd_d256.cu", "sm103_ptx.cuh", "bounded_wait.cuh", "fa_internal.cuh", "tma_map.cuh"),
+    "bwd_simt_kernel": ("bwd_simt.cu", "sm103_ptx.cuh", "fa_internal.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str = "bwd_sm103_kernel") -> str:
+    """Hash of a main kernel's sources (see KERNEL_SOURCES)."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("bwd_sm103.cu", "sm103_ptx.cuh", "bounded_wait.cuh", "fa_internal.cuh"):
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "flashattention_backward_preprocess_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def main_kernel_traffic(workload: str, deterministic: bool = False):
+def main_kernel_traffic(workload: str, deterministic: bool = False, kernel: str = "bwd_sm103_kernel"):
     """DRAM bytes (read + write) per main-kernel launch from the committed ncu summary, or None
     when the kernel's sources changed since the counters were taken.  The counters are those of
     the default (non-deterministic) kernel instance: a deterministic run gets None."""
@@ -165,19 +173,27 @@ def main_kernel_traffic(workload: str, deterministic: bool = False):
             d = json.load(f)
     except Exception:
         return None
-    if d.get("kernel_sha") != kernel_source_hash():
+    k = d.get("kernels", {}).get(kernel)
+    if not k or k.get("sha") != kernel_source_hash(kernel):
         return None
-    return d.get("bytes_per_launch", {}).get(workload)
+    return k.get("bytes_per_launch", {}).get(workload)
 
 
 FP32_SMS = 152  # GB300 streaming multiprocessors (each 128 fp32 FMA lanes)
 
 
-def main_kernel_name(w, det: bool) -> str:
+def main_kernel_family(w) -> str:
     """The main backward kernel fa_bwd runs for a workload (the library's dispatch)."""
     if w.dtype == "f32":
+        return "bwd_simt_kernel"
+    return "bwd_d256_kernel" if w.d == 256 else "bwd_sm103_kernel"
+
+
+def main_kernel_name(w, det: bool) -> str:
+    fam = main_kernel_family(w)
+    if fam == "bwd_simt_kernel":
         return f"bwd_simt_kernel<f32,{w.d}>"
-    if w.d == 256:
+    if fam == "bwd_d256_kernel":
         return f"bwd_d256_kernel<{w.dtype}>"
     return f"bwd_sm103_kernel<{w.dtype},{128 if w.d > 64 else 64},{'det' if det else 'default'}>"
 
@@ -383,7 +399,8 @@ def main():
         sm_mhz = float(peaks.get("sm_max_mhz", 2070.0))
         peak = FP32_SMS * 128 * 2 * sm_mhz * 1e6 / 1e12
         roofline = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": None,
+                    "frac": achieved / peak,
+                    "traffic": main_kernel_traffic(w.name, det, "bwd_simt_kernel"),
                     "peak_source": f"{FP32_SMS} SMs x 128 fp32 FMA lanes x 2 flops x {sm_mhz:.0f} MHz "
                                    f"({peak_src} sm_max_mhz)",
                     "kernel": kernel, "kernel_ms": main_ms,
@@ -391,7 +408,7 @@ def main():
                     "step_frac": (flops / (ms / 1e3) / 1e12) / peak}
     else:
         peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-        traffic = main_kernel_traffic(w.name, det)
+        traffic = main_kernel_traffic(w.name, det, main_kernel_family(w))
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": traffic, "peak_source": f"{peak_src} bf16_tflops (burst)",
                     "kernel": kernel, "kernel_ms": main_ms,
