@@ -14,6 +14,10 @@
 // (ty, tx) of the 16 x 16 grid owns rows ty + 16r and columns tx + 16c of S / dP, key rows
 // ty + 16r and 4-column groups tx + 16g of dK / dV, query rows ty + 16r and the same column
 // groups of dQ.  scale is applied to dK here and to dQ in the finalisation kernel.
+// For fp32 outputs a key tile can be split over two CTAs (small grids, long causal key
+// tiles): each takes one half of the tile's (head, query tile) iterations and adds its dK / dV
+// partial sums into the zeroed outputs with fp32 reductions.  Two addends onto zero give the
+// same bits in either order, so dK and dV stay reproducible.
 #include <math.h>
 
 #include "fa_internal.cuh"
@@ -63,7 +67,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) bwd_simt_kernel(
     const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
     const T* __restrict__ dO, const float* __restrict__ lse2, const float* __restrict__ Dws,
-    float* __restrict__ dqacc, T* __restrict__ dK, T* __restrict__ dV, Shape s) {
+    float* __restrict__ dqacc, T* __restrict__ dK, T* __restrict__ dV, Shape s, int split) {
     using C = SCfg<D>;
     constexpr int BN = C::BN, BM = C::BM, LD = C::LD, LP = C::LP, TR = C::TR, TC = C::TC, NG = C::NG;
     extern __shared__ float4 smem4[];
@@ -78,11 +82,13 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_kernel(
     float* sDd = sL + BM;           // [BM] D
 
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-    // blockIdx.x = key tile x (batch, kv head), key tile outer: with causal masking the key
-    // tiles with the most query rows start first
+    // blockIdx.x = (key tile x (batch, kv head), key tile outer: with causal masking the key
+    // tiles with the most query rows start first) x the split rank
     const int groups = s.B * s.H_kv;
-    const int n0 = (blockIdx.x / groups) * BN;
-    const int bkv = blockIdx.x % groups;
+    const int rank = (int)(blockIdx.x % (unsigned)split);
+    const int item = (int)(blockIdx.x / (unsigned)split);
+    const int n0 = (item / groups) * BN;
+    const int bkv = item % groups;
     const int b = bkv / s.H_kv, hk = bkv % s.H_kv;
     const int g = s.H / s.H_kv;
     const int off = s.S_k - s.S_q;  // query i sits at key position i + off
@@ -100,14 +106,19 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_kernel(
 #pragma unroll
             for (int u = 0; u < 4; ++u) accV[r][q][u] = accK[r][q][u] = 0.f;
 
-    // query rows [i_begin, i_end) see a key of this tile
+    // query rows [i_begin, i_end) see a key of this tile: nq query tiles per head, this CTA's
+    // share of the g * nq (head, query tile) iterations is [it_lo, it_hi)
     int i_begin, i_end;
     query_range(s, n0, min(n0 + BN, s.S_k), i_begin, i_end);
     const int m_first = i_begin / BM * BM;
+    const int nq = i_end > i_begin ? (i_end - m_first + BM - 1) / BM : 0;
+    const int it_lo = g * nq * rank / split, it_hi = g * nq * (rank + 1) / split;
 
-    for (int hh = 0; hh < g; ++hh) {
-        const int bh = b * s.H + hk * g + hh;
-        for (int m0 = m_first; m0 < i_end; m0 += BM) {
+    {
+        for (int it = it_lo; it < it_hi; ++it) {
+            const int hh = it / nq;
+            const int bh = b * s.H + hk * g + hh;
+            const int m0 = m_first + (it % nq) * BM;
             const int rows = min(BM, s.S_q - m0);
             __syncthreads();  // the previous step's reads of sQ, sdO, sP, sdS are done
             stage_rows<T, D>(sQ, Q + ((size_t)bh * s.S_q + m0) * D, rows, BM);
@@ -239,7 +250,7 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_kernel(
             }
         }
     }
-    // ---- dK (scaled) and dV rows of this tile
+    // ---- dK (scaled) and dV rows of this tile (added into the zeroed fp32 outputs when split)
 #pragma unroll
     for (int r = 0; r < TC; ++r) {
         const int j = n0 + ty + 16 * r;
@@ -250,6 +261,15 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_kernel(
             if (!(NG * 16 * 4 == D || f < D / 4)) continue;
             T* pv = dV + ((size_t)bkv * s.S_k + j) * D + 4 * f;
             T* pk = dK + ((size_t)bkv * s.S_k + j) * D + 4 * f;
+            if constexpr (sizeof(T) == 4) {
+                if (split > 1) {
+                    ptx::red_add_v4(reinterpret_cast<float*>(pv), accV[r][q][0], accV[r][q][1], accV[r][q][2],
+                                    accV[r][q][3]);
+                    ptx::red_add_v4(reinterpret_cast<float*>(pk), accK[r][q][0] * s.scale, accK[r][q][1] * s.scale,
+                                    accK[r][q][2] * s.scale, accK[r][q][3] * s.scale);
+                    continue;
+                }
+            }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 pv[u] = TypeTraits<T>::from_f32(accV[r][q][u]);
@@ -350,11 +370,31 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, const void* dO
     auto kern = bwd_simt_kernel<T, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
-    const long grid = (long)((s.S_k + C::BN - 1) / C::BN) * s.B * s.H_kv;
+    // fp32 outputs: two CTAs per key tile when the grid would not fill the SMs or its heaviest
+    // causal CTA outlasts the per-SM share (in both modes, so that dK and dV do not depend on
+    // the mode: two partial sums added onto zero give the same bits in either order)
+    int split = 1;
+    if (sizeof(T) == 4) {
+        const long ctas = (long)((s.S_k + C::BN - 1) / C::BN) * s.B * s.H_kv;
+        static int sms = 0;
+        if (sms == 0) {
+            int dev = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+                sms = 148;
+        }
+        if (ctas < sms || key_tile_split(s, C::BN, C::BM) == 2) split = 2;
+    }
+    if (split > 1) {
+        const size_t bytes = (size_t)s.B * s.H_kv * s.S_k * D * sizeof(T);
+        if ((e = cudaMemsetAsync(dK, 0, bytes, st)) != cudaSuccess) return e;
+        if ((e = cudaMemsetAsync(dV, 0, bytes, st)) != cudaSuccess) return e;
+    }
+    const long grid = (long)((s.S_k + C::BN - 1) / C::BN) * s.B * s.H_kv * split;
     kern<<<(unsigned)grid, kThreads, C::SMEM, st>>>(static_cast<const T*>(Q), static_cast<const T*>(K),
                                                     static_cast<const T*>(V), static_cast<const T*>(dO),
                                                     ws.lse2, ws.Dws, skip_dq ? nullptr : ws.dqacc,
-                                                    static_cast<T*>(dK), static_cast<T*>(dV), s);
+                                                    static_cast<T*>(dK), static_cast<T*>(dV), s, split);
     return cudaGetLastError();
 }
 
