@@ -93,7 +93,7 @@ struct Cfg {
     static constexpr uint32_t OFF_LSE = OFF_DS + NDS * kdS_B;
     static constexpr uint32_t OFF_DD = OFF_LSE + STAGES * BM * 4;
     static constexpr uint32_t OFF_BAR = OFF_DD + STAGES * BM * 4;
-    static constexpr uint32_t kNumBars = 23 + 2 * STAGES;  // B_STAGE0 + 2 * STAGES
+    static constexpr uint32_t kNumBars = 23 + 4 * STAGES;  // B_STAGE0 + 4 * STAGES
     static constexpr uint32_t OFF_MISC = OFF_BAR + kNumBars * 8;
     static constexpr uint32_t SMEM = OFF_MISC + 16;
     static constexpr uint32_t TM_DV = 0, TM_DK = D, TM_BUF0 = 2 * D;
@@ -118,7 +118,8 @@ enum {
     B_FINAL,       // MMA shutdown
     B_FINAL_A,     // S / dP issuer shutdown (two issuers)
     B_YFREE,       // two issuers: the dK product of the iteration that used buffer k as Y is done
-    B_STAGE0 = B_YFREE + 3  // then STAGES "full" barriers, then STAGES "empty" barriers
+    B_STAGE0 = B_YFREE + 3  // then the stage ring: STAGES "full" and STAGES "empty" barriers for
+                            // the Q tiles (with the LSE rows), then the same for the dO tiles (with D)
 };
 
 struct Params {
@@ -172,12 +173,20 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
     const uint32_t sbase = ptx::smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // the dQ finalisation (launched as a programmatic dependent) may be scheduled once every
+    // CTA of this grid has started; it waits for this grid to complete
+    ptx::griddep_launch_dependents();
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 4);
     uint32_t* ticket_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 8);
     auto bar = [&](int i) { return sbase + C::OFF_BAR + 8u * (uint32_t)i; };
-    auto bar_full = [&](int s) { return bar(B_STAGE0 + s); };
-    auto bar_empty = [&](int s) { return bar(B_STAGE0 + C::STAGES + s); };
+    // Q and dO stages are loaded and released separately: at d = 128 the drain stages half of
+    // dQ(i) in the dO tile, and the Q tile of iteration i+2 (for S(i+2) and the P pass) need not
+    // wait until TMA has read that out
+    auto full_q = [&](int s) { return bar(B_STAGE0 + s); };
+    auto empty_q = [&](int s) { return bar(B_STAGE0 + C::STAGES + s); };
+    auto full_do = [&](int s) { return bar(B_STAGE0 + 2 * C::STAGES + s); };
+    auto empty_do = [&](int s) { return bar(B_STAGE0 + 3 * C::STAGES + s); };
 
     if (threadIdx.x == 0) {
         if ((sbase & 1023u) != 0) atomicOr(p.err, kErrSmemAlign);
@@ -186,7 +195,7 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
             uint32_t count = ((i >= B_P_READY && i < B_P_READY + 3) || i == B_DS_READY) ? (uint32_t)kNumSoftWarps
                              : (i == B_DQ_EMPTY || i == B_DQ_STAGED || i == B_DQ_STAGED + 1) ? 4u
                                                                : 1u;
-            if (D == 128 && i >= B_STAGE0 + C::STAGES) count = 2;  // stage "empty": MMA + drain
+            if (D == 128 && i >= B_STAGE0 + 3 * C::STAGES) count = 2;  // dO stage "empty": MMA + drain
             ptx::mbar_init(bar(i), count);
         }
         ptx::fence_mbar_init();
@@ -268,8 +277,8 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
     };
     // Bulk reduce-adds of the dQ tile staged for iteration it (one thread), then the
     // releases once TMA has read each staging area: the dS tile (B_DS_EMPTY) and, at
-    // d = 128, the Q / dO stage, whose second arrival (after the MMA warp's, once the dK
-    // product that reads Q is done) lets the next load in.
+    // d = 128, the dO stage, whose second arrival (after the MMA warp's, once the dK
+    // product is done) lets the next dO load in.
     auto reduce_staged = [&](int s, int tile, int bh, int m0, bool add) {
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {  // one bulk group per staging area, dS tile first
@@ -288,7 +297,7 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
             ptx::bulk_wait_read_1();  // the dS-tile group (the older one) was read
             ptx::mbar_arrive(bar(B_DS_EMPTY + tile));
             ptx::bulk_wait_read_all();
-            ptx::mbar_arrive(bar_empty(s));  // second of two arrivals (MMA commit after dK)
+            ptx::mbar_arrive(empty_do(s));  // second of two arrivals (MMA commit after dK)
         } else {
             ptx::bulk_wait_read_all();
             ptx::mbar_arrive(bar(B_DS_EMPTY + tile));
@@ -298,36 +307,66 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
 
     if (warp == kWarpTma) {
         // ------------------------------------------------------------ producer
+        // One thread loads K, V, then the Q tiles (with the LSE rows) and the dO tiles (with
+        // D) of the stage ring, each as soon as its own slot is free, polling both "empty"
+        // barriers without blocking on either.
         if (lane == 0 && !*abort_flag) {
+            // K and V are read by this CTA alone: their lines go first when L2 needs room (the dQ
+            // accumulator lines the reduce-adds update stay; measured 0.6 % faster)
+            const uint64_t kv_pol = ptx::policy_evict_first();
             ptx::mbar_arrive_expect_tx(bar(B_KV), 2 * C::kTileK_B);
             for (int x = 0; x < C::BOXES; ++x) {
-                ptx::tma_load_3d(sbase + C::OFF_K + x * C::kBoxK_B, &tmK, x * 64, n0, bkv, bar(B_KV));
-                ptx::tma_load_3d(sbase + C::OFF_V + x * C::kBoxK_B, &tmV, x * 64, n0, bkv, bar(B_KV));
+                ptx::tma_load_3d_hint(sbase + C::OFF_K + x * C::kBoxK_B, &tmK, x * 64, n0, bkv, bar(B_KV), kv_pol);
+                ptx::tma_load_3d_hint(sbase + C::OFF_V + x * C::kBoxK_B, &tmV, x * 64, n0, bkv, bar(B_KV), kv_pol);
             }
-            int issued = 0;
-            for (int it = 0; it < n_it; ++it) {
+            // launched as a programmatic dependent of the preprocess pass: the LSE copy and D it
+            // writes are read from here on
+            ptx::griddep_wait();
+            ptx::fence_proxy_async_global();
+            auto load = [&](bool is_q, int it) {
                 const int s = it % C::STAGES;
-                if (it >= C::STAGES &&
-                    !wait_bar(bar_empty(s), ((it / C::STAGES) - 1) & 1, abort_flag, p.err))
-                    break;
                 int bh, m0;
                 iter_coords(it, bh, m0);
-                ptx::mbar_arrive_expect_tx(bar_full(s), 2 * C::kTileQ_B + 2 * BM * 4);
-                for (int x = 0; x < C::BOXES; ++x) {
-                    ptx::tma_load_3d(sbase + C::OFF_Q + s * C::kTileQ_B + x * C::kBoxQ_B, &tmQ, x * 64,
-                                     m0, bh, bar_full(s));
-                    ptx::tma_load_3d(sbase + C::OFF_DO + s * C::kTileQ_B + x * C::kBoxQ_B, &tmdO,
-                                     x * 64, m0, bh, bar_full(s));
+                const uint32_t full = is_q ? full_q(s) : full_do(s);
+                const uint32_t tile = sbase + (is_q ? C::OFF_Q : C::OFF_DO) + s * C::kTileQ_B;
+                ptx::mbar_arrive_expect_tx(full, C::kTileQ_B + BM * 4);
+                for (int x = 0; x < C::BOXES; ++x)
+                    ptx::tma_load_3d(tile + x * C::kBoxQ_B, is_q ? &tmQ : &tmdO, x * 64, m0, bh, full);
+                ptx::bulk_load(sbase + (is_q ? C::OFF_LSE : C::OFF_DD) + s * BM * 4,
+                               (is_q ? p.lse2 : p.Dws) + (size_t)bh * p.S_q_pad + m0, BM * 4, full);
+            };
+            int iq = 0, id = 0;  // loads issued
+            uint64_t t0 = ptx::globaltimer();
+            uint32_t spins = 0;
+            while (iq < n_it || id < n_it) {
+                bool progress = false;
+                if (iq < n_it && (iq < C::STAGES || ptx::mbar_test_wait(empty_q(iq % C::STAGES),
+                                                                        ((iq / C::STAGES) - 1) & 1))) {
+                    load(true, iq++);
+                    progress = true;
                 }
-                const size_t row0 = (size_t)bh * p.S_q_pad + m0;
-                ptx::bulk_load(sbase + C::OFF_LSE + s * BM * 4, p.lse2 + row0, BM * 4, bar_full(s));
-                ptx::bulk_load(sbase + C::OFF_DD + s * BM * 4, p.Dws + row0, BM * 4, bar_full(s));
-                issued = it + 1;
+                if (id < n_it && (id < C::STAGES || ptx::mbar_test_wait(empty_do(id % C::STAGES),
+                                                                        ((id / C::STAGES) - 1) & 1))) {
+                    load(false, id++);
+                    progress = true;
+                }
+                if (progress) {
+                    t0 = ptx::globaltimer();
+                } else if (++spins % 64 == 0) {
+                    if (*abort_flag) break;
+                    if (ptx::globaltimer() - t0 > kWaitLimitNs) {
+                        *abort_flag = 1;
+                        atomicOr(p.err, kErrTimeout);
+                        break;
+                    }
+                }
             }
             // never leave copies in flight into shared memory that is about to be released
             drain_wait(bar(B_KV), 0);
-            for (int it = issued - C::STAGES < 0 ? 0 : issued - C::STAGES; it < issued; ++it)
-                drain_wait(bar_full(it % C::STAGES), (it / C::STAGES) & 1);
+            for (int it = iq - C::STAGES < 0 ? 0 : iq - C::STAGES; it < iq; ++it)
+                drain_wait(full_q(it % C::STAGES), (it / C::STAGES) & 1);
+            for (int it = id - C::STAGES < 0 ? 0 : id - C::STAGES; it < id; ++it)
+                drain_wait(full_do(it % C::STAGES), (it / C::STAGES) & 1);
         }
     } else if (warp == kWarpMma || (NBUF == 3 && warp == kWarpMma2)) {
         // ------------------------------------------------------------ MMA issuers
@@ -360,11 +399,15 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
             bool ok = true;
             if (issue_sd) {
                 ok = wait_bar(bar(B_KV), 0, abort_flag, p.err);
-                if (ok) ok = wait_bar(bar_full(0), 0, abort_flag, p.err);
+                if (ok) ok = wait_bar(full_q(0), 0, abort_flag, p.err);
                 if (ok) {
                     ptx::tc_fence_after();
                     gemm_sd(tm_buf0 + 128 * xb(0), sK, sbase + C::OFF_Q);
                     ptx::mma_commit(bar(B_S_FULL + sp_slot(0)));
+                }
+                if (ok) ok = wait_bar(full_do(0), 0, abort_flag, p.err);
+                if (ok) {
+                    ptx::tc_fence_after();
                     gemm_sd(tm_buf0 + 128 * yb(0), sV, sbase + C::OFF_DO);
                     ptx::mma_commit(bar(B_DP_FULL));
                 }
@@ -381,7 +424,7 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
                     if (it + 1 < n_it) {
                         // S(i+1) into yb(i-1) once Q(i+1) is in and the dK product of iteration
                         // i-1 stopped reading dS(i-1) from it (the first iteration's is unused)
-                        if (!(ok = wait_bar(bar_full(s1), ((it + 1) / C::STAGES) & 1, abort_flag, p.err))) break;
+                        if (!(ok = wait_bar(full_q(s1), ((it + 1) / C::STAGES) & 1, abort_flag, p.err))) break;
                         if (it > 0 &&
                             !(ok = wait_bar(bar(B_YFREE + yb(it - 1)), ((it - 1) / 3) & 1, abort_flag, p.err)))
                             break;
@@ -390,6 +433,7 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
                         ptx::mma_commit(bar(B_S_FULL + sp_slot(it + 1)));
                         // dP(i+1) into xb(i) once dQ(i) left it
                         if (!(ok = wait_bar(bar(B_DQ_EMPTY), it & 1, abort_flag, p.err))) break;
+                        if (!(ok = wait_bar(full_do(s1), ((it + 1) / C::STAGES) & 1, abort_flag, p.err))) break;
                         ptx::tc_fence_after();
                         gemm_sd(X, sV, sbase + C::OFF_DO + s1 * C::kTileQ_B);
                         ptx::mma_commit(bar(B_DP_FULL));
@@ -422,18 +466,20 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
                                 ID_KV, (it > 0 || k > 0) ? 1u : 0u);
                 ptx::mma_commit(bar(NBUF == 3 ? B_YFREE + yb(it) : B_G4));
                 // Q(i), dO(i) no longer read by MMAs (S(i) and dP(i) completed before dS(i);
-                // for d = 128 the stage is free only once the drain also arrived: it stages
+                // for d = 128 the dO stage is free only once the drain also arrived: it stages
                 // half of dQ(i) in the dO tile)
-                ptx::mma_commit(bar_empty(s));
+                ptx::mma_commit(empty_q(s));
+                ptx::mma_commit(empty_do(s));
                 if (NBUF == 2 && it + 1 < n_it) {
                     // S(i+1) into Y once the dK product stopped reading dS(i) from it
-                    if (!(ok = wait_bar(bar_full(s1), ((it + 1) / C::STAGES) & 1, abort_flag, p.err))) break;
+                    if (!(ok = wait_bar(full_q(s1), ((it + 1) / C::STAGES) & 1, abort_flag, p.err))) break;
                     if (!(ok = wait_bar(bar(B_G4), it & 1, abort_flag, p.err))) break;
                     ptx::tc_fence_after();
                     gemm_sd(Y, sK, sbase + C::OFF_Q + s1 * C::kTileQ_B);
                     ptx::mma_commit(bar(B_S_FULL + sp_slot(it + 1)));
                     // dP(i+1) into X once dQ(i) left it
                     if (!(ok = wait_bar(bar(B_DQ_EMPTY), it & 1, abort_flag, p.err))) break;
+                    if (!(ok = wait_bar(full_do(s1), ((it + 1) / C::STAGES) & 1, abort_flag, p.err))) break;
                     ptx::tc_fence_after();
                     gemm_sd(X, sV, sbase + C::OFF_DO + s1 * C::kTileQ_B);
                     ptx::mma_commit(bar(B_DP_FULL));
@@ -484,7 +530,7 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
             const bool mask_tile = __any_sync(0xffffffffu, !full);
             const float* sl = reinterpret_cast<const float*>(smem + C::OFF_LSE + s * BM * 4) + qh;
             const float* sd = reinterpret_cast<const float*>(smem + C::OFF_DD + s * BM * 4) + qh;
-            if (!(ok = wait_bar_warp(bar_full(s), (it / C::STAGES) & 1, abort_flag, p.err))) break;
+            if (!(ok = wait_bar_warp(full_q(s), (it / C::STAGES) & 1, abort_flag, p.err))) break;
             if (!(ok = wait_bar_warp(bar(B_S_FULL + sp_slot(it)), sp_par(it), abort_flag, p.err))) break;
             ptx::tc_fence_after();
             // P = exp2(S * scale*log2e - LSE*log2e), packed to 16 bits in place.  Masking is
@@ -532,6 +578,7 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
             // dS = P * (dP - D): packed in place into this warp's first 32 columns of Y for
             // the dK product, and into the shared dS tile for dQ.
             if (!(ok = wait_bar_warp(bar(B_DP_FULL), it & 1, abort_flag, p.err))) break;
+            if (!(ok = wait_bar_warp(full_do(s), (it / C::STAGES) & 1, abort_flag, p.err))) break;  // D row
             // the dS tile of this iteration was last used NDS iterations ago
             if (it >= NDS &&
                 !(ok = wait_bar_warp(bar(B_DS_EMPTY + dt(it)), ((it - NDS) / NDS) & 1, abort_flag, p.err)))
@@ -621,6 +668,8 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
         // after the stage's previous reduce had read it.
         const int t = (warp - kWarpDrain0) * 32 + lane;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        ptx::griddep_wait();  // the accumulator was zeroed by the preprocess pass
+        ptx::fence_proxy_async_global();
         bool ok = !*abort_flag;
         for (int it = 0; ok && it < n_it; ++it) {
             const int s = it % C::STAGES;
@@ -674,6 +723,8 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
         // holds up the drain (measured 9 % faster in deterministic mode than in the drain's
         // issuer; the default mode keeps the issuer, 2-4 % faster there).
         if (lane == 0 && det) {
+            ptx::griddep_wait();
+            ptx::fence_proxy_async_global();
             bool ok = !*abort_flag;
             unsigned int* prev_sem = nullptr;  // turn to pass on once complete
             unsigned int prev_turn = 0;
@@ -892,22 +943,31 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, const void* dO
     if (e != cudaSuccess) return e;
     const long grid = (long)((s.S_k + BN - 1) / BN) * s.B * s.H_kv * split;
     const int threads = threads_for(ws.dq_sem != nullptr, D);
-    if (split == 1) {
-        kern<<<(unsigned)grid, threads, C::SMEM, st>>>(tq, tk, tv, tdo, tdq, p);
-        return cudaGetLastError();
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)split;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (split > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)split;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (ws.dq_sem == nullptr) {
+        // programmatic dependent launch: the set-up (barriers, TMEM, K / V loads) overlaps the
+        // end of the preprocess pass; the roles that read what it wrote wait for it
+        // (deterministic calls keep the full dependency: their turn counters and ticket are
+        // reset by a memset ahead of the preprocess pass)
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = (unsigned)na;
     return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, tdo, tdq, p);
 }
 

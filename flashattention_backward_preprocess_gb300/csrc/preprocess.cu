@@ -19,6 +19,7 @@
 #include <math.h>
 
 #include "fa_internal.cuh"
+#include "sm103_ptx.cuh"
 
 namespace fa {
 namespace {
@@ -38,6 +39,9 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const T* __restrict__ d
                                                          float* __restrict__ lse2,
                                                          float* __restrict__ dqacc, int BH,
                                                          int S_q, int rows_stride) {
+    // the main kernel may start its set-up while the last blocks of this pass run (it waits
+    // for this grid before it reads D, the LSE copy or the accumulator)
+    ptx::griddep_launch_dependents();
     constexpr int VEC = 16 / sizeof(T);  // elements per 16-byte chunk
     constexpr int CPR = D / VEC;         // 16-byte chunks per row
     constexpr int LPR = lanes_per_row(CPR);
@@ -88,7 +92,9 @@ template <typename T>
 __global__ void __launch_bounds__(256) dq_finalize_kernel(const float* __restrict__ acc,
                                                           T* __restrict__ dQ, size_t n8,
                                                           float scale) {
-    // n8 = number of 8-element groups; d is a multiple of 8 so rows never split.
+    // n8 = number of 8-element groups; d is a multiple of 8 so rows never split.  Launched
+    // as a programmatic dependent of the main kernel: wait until it has completed.
+    ptx::griddep_wait();
     for (size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x; g < n8;
          g += (size_t)gridDim.x * blockDim.x) {
         // streaming loads and stores (evict first): the lines of the accumulator the main
@@ -133,8 +139,19 @@ cudaError_t launch_fin_t(const float* acc, void* dQ, const Shape& s, cudaStream_
     const size_t cap = (size_t)sms * 8;
     if (grid > cap) grid = cap;
     if (grid == 0) grid = 1;
-    dq_finalize_kernel<T><<<(unsigned)grid, 256, 0, st>>>(acc, static_cast<T*>(dQ), n8, s.scale);
-    return cudaGetLastError();
+    // programmatic dependent launch: the blocks are scheduled while the main kernel's last
+    // CTAs finish and start converting as soon as it has completed
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dq_finalize_kernel<T>, acc, static_cast<T*>(dQ), n8, s.scale);
 }
 
 }  // namespace
