@@ -180,13 +180,15 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 4);
     uint32_t* ticket_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 8);
     auto bar = [&](int i) { return sbase + C::OFF_BAR + 8u * (uint32_t)i; };
-    // Q and dO stages are loaded and released separately: at d = 128 the drain stages half of
-    // dQ(i) in the dO tile, and the Q tile of iteration i+2 (for S(i+2) and the P pass) need not
-    // wait until TMA has read that out
+    // At d = 128 the Q and dO stages are loaded and released separately: the drain stages half
+    // of dQ(i) in the dO tile, and the Q tile of iteration i+2 (for S(i+2) and the P pass) need
+    // not wait until TMA has read that out.  At d = 64 both tiles of an iteration share one
+    // full and one empty barrier (measured 3 % faster there).
+    constexpr bool kSplitRing = D == 128;
     auto full_q = [&](int s) { return bar(B_STAGE0 + s); };
     auto empty_q = [&](int s) { return bar(B_STAGE0 + C::STAGES + s); };
-    auto full_do = [&](int s) { return bar(B_STAGE0 + 2 * C::STAGES + s); };
-    auto empty_do = [&](int s) { return bar(B_STAGE0 + 3 * C::STAGES + s); };
+    auto full_do = [&](int s) { return kSplitRing ? bar(B_STAGE0 + 2 * C::STAGES + s) : full_q(s); };
+    auto empty_do = [&](int s) { return kSplitRing ? bar(B_STAGE0 + 3 * C::STAGES + s) : empty_q(s); };
 
     if (threadIdx.x == 0) {
         if ((sbase & 1023u) != 0) atomicOr(p.err, kErrSmemAlign);
@@ -323,17 +325,23 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
             // writes are read from here on
             ptx::griddep_wait();
             ptx::fence_proxy_async_global();
+            // the lse2 and D rows travel with the Q tile (the P pass waits for it; the dS pass
+            // comes later in the same iteration and the Q stage is released after the dK product)
             auto load = [&](bool is_q, int it) {
                 const int s = it % C::STAGES;
                 int bh, m0;
                 iter_coords(it, bh, m0);
                 const uint32_t full = is_q ? full_q(s) : full_do(s);
-                const uint32_t tile = sbase + (is_q ? C::OFF_Q : C::OFF_DO) + s * C::kTileQ_B;
-                ptx::mbar_arrive_expect_tx(full, C::kTileQ_B + BM * 4);
+                const uint32_t bytes = is_q ? C::kTileQ_B * (kSplitRing ? 1 : 2) + 2 * BM * 4 : C::kTileQ_B;
+                if (is_q || kSplitRing) ptx::mbar_arrive_expect_tx(full, bytes);
                 for (int x = 0; x < C::BOXES; ++x)
-                    ptx::tma_load_3d(tile + x * C::kBoxQ_B, is_q ? &tmQ : &tmdO, x * 64, m0, bh, full);
-                ptx::bulk_load(sbase + (is_q ? C::OFF_LSE : C::OFF_DD) + s * BM * 4,
-                               (is_q ? p.lse2 : p.Dws) + (size_t)bh * p.S_q_pad + m0, BM * 4, full);
+                    ptx::tma_load_3d(sbase + (is_q ? C::OFF_Q : C::OFF_DO) + s * C::kTileQ_B + x * C::kBoxQ_B,
+                                     is_q ? &tmQ : &tmdO, x * 64, m0, bh, full);
+                if (is_q) {
+                    const size_t row0 = (size_t)bh * p.S_q_pad + m0;
+                    ptx::bulk_load(sbase + C::OFF_LSE + s * BM * 4, p.lse2 + row0, BM * 4, full);
+                    ptx::bulk_load(sbase + C::OFF_DD + s * BM * 4, p.Dws + row0, BM * 4, full);
+                }
             };
             int iq = 0, id = 0;  // loads issued
             uint64_t t0 = ptx::globaltimer();
@@ -342,11 +350,13 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
                 bool progress = false;
                 if (iq < n_it && (iq < C::STAGES || ptx::mbar_test_wait(empty_q(iq % C::STAGES),
                                                                         ((iq / C::STAGES) - 1) & 1))) {
-                    load(true, iq++);
+                    load(true, iq);
+                    if (!kSplitRing) load(false, id++);  // one shared barrier: both tiles at once
+                    ++iq;
                     progress = true;
                 }
-                if (id < n_it && (id < C::STAGES || ptx::mbar_test_wait(empty_do(id % C::STAGES),
-                                                                        ((id / C::STAGES) - 1) & 1))) {
+                if (kSplitRing && id < n_it &&
+                    (id < C::STAGES || ptx::mbar_test_wait(empty_do(id % C::STAGES), ((id / C::STAGES) - 1) & 1))) {
                     load(false, id++);
                     progress = true;
                 }
@@ -365,8 +375,9 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
             drain_wait(bar(B_KV), 0);
             for (int it = iq - C::STAGES < 0 ? 0 : iq - C::STAGES; it < iq; ++it)
                 drain_wait(full_q(it % C::STAGES), (it / C::STAGES) & 1);
-            for (int it = id - C::STAGES < 0 ? 0 : id - C::STAGES; it < id; ++it)
-                drain_wait(full_do(it % C::STAGES), (it / C::STAGES) & 1);
+            if (kSplitRing)
+                for (int it = id - C::STAGES < 0 ? 0 : id - C::STAGES; it < id; ++it)
+                    drain_wait(full_do(it % C::STAGES), (it / C::STAGES) & 1);
         }
     } else if (warp == kWarpMma || (NBUF == 3 && warp == kWarpMma2)) {
         // ------------------------------------------------------------ MMA issuers
@@ -469,7 +480,7 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
                 // for d = 128 the dO stage is free only once the drain also arrived: it stages
                 // half of dQ(i) in the dO tile)
                 ptx::mma_commit(empty_q(s));
-                ptx::mma_commit(empty_do(s));
+                if (kSplitRing) ptx::mma_commit(empty_do(s));
                 if (NBUF == 2 && it + 1 < n_it) {
                     // S(i+1) into Y once the dK product stopped reading dS(i) from it
                     if (!(ok = wait_bar(full_q(s1), ((it + 1) / C::STAGES) & 1, abort_flag, p.err))) break;
@@ -578,7 +589,6 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
             // dS = P * (dP - D): packed in place into this warp's first 32 columns of Y for
             // the dK product, and into the shared dS tile for dQ.
             if (!(ok = wait_bar_warp(bar(B_DP_FULL), it & 1, abort_flag, p.err))) break;
-            if (!(ok = wait_bar_warp(full_do(s), (it / C::STAGES) & 1, abort_flag, p.err))) break;  // D row
             // the dS tile of this iteration was last used NDS iterations ago
             if (it >= NDS &&
                 !(ok = wait_bar_warp(bar(B_DS_EMPTY + dt(it)), ((it - NDS) / NDS) & 1, abort_flag, p.err)))
