@@ -13,10 +13,11 @@ at a random later time.  It checks that
   * every wait sees its barrier either at the awaited phase (blocks) or one past it (passes),
   * no schedule deadlocks,
   * every read of a TMEM buffer or shared tile finds the data the reader expects.
-It covers the configurations the backward has: two TMEM buffers and one MMA issuer (d = 128), three
-buffers, two dS tiles and two issuers (d = 64), each with the drain's first thread or (the
-deterministic instance) a reduce warp issuing the dQ reduce-adds; and the forward kernel
-(csrc/fwd_sm103.cu) with three S buffers (d <= 128) or two (d = 256).
+It covers the configurations the backward has: two TMEM buffers, one MMA issuer and separate Q and
+dO rings (d = 128), three buffers, two dS tiles, two issuers and one ring for both tiles (d = 64),
+each with the drain's first thread or (the deterministic instance) a reduce warp issuing the dQ
+reduce-adds; and the forward kernel (csrc/fwd_sm103.cu) with three S buffers (d <= 128) or two
+(d = 256), one item per CTA or (the persistent kernel) a sequence of items.
 
 The model is not generated from the kernel: a change to the kernel's protocol needs the same change
 here, and this test then says whether the new protocol is sound.
@@ -52,7 +53,10 @@ class Model:
         self.d = d
         self.split = self.NBUF == 3          # two MMA issuers
         self.use_red = det                    # reduce warp (deterministic instance)
-        cnt_empty = 2 if d == 128 else 1      # stage "empty": MMA commit (+ drain / reduce warp at d = 128)
+        # d = 128: separate Q and dO rings (the drain stages half of dQ in the dO tile, whose
+        # "empty" then takes the MMA commit and the drain's / reduce warp's arrival); d = 64: one
+        # pair of barriers per stage for both tiles
+        self.split_ring = d == 128
         self.bars = {}
 
         def bar(name, count=1):
@@ -69,8 +73,14 @@ class Model:
             bar(f"DS_EMPTY{t}")
             bar(f"DQ_STAGED{t}")
         for s in range(self.STAGES):
-            bar(f"FULL{s}")
-            bar(f"EMPTY{s}", cnt_empty)
+            bar(f"FULLQ{s}")
+            bar(f"EMPTYQ{s}")
+            if self.split_ring:
+                bar(f"FULLDO{s}")
+                bar(f"EMPTYDO{s}", 2)
+            else:  # the same barriers serve both tiles
+                self.bars[f"FULLDO{s}"] = self.bars[f"FULLQ{s}"]
+                self.bars[f"EMPTYDO{s}"] = self.bars[f"EMPTYQ{s}"]
         self.res = {}            # resource -> label of its content
         self.mma_q = {}          # issuer -> list of queued ops (executed in order)
         self.async_ops = []      # TMA loads and bulk reads in flight
@@ -116,15 +126,27 @@ class Model:
 
     # ---- roles
     def producer(self):
+        """K, V, then the Q tiles with the lse2 / D rows (and, one shared ring, the dO tiles)."""
         self.async_ops.append(("tma", [("K", "K"), ("V", "V")], "KV"))
         for it in range(self.n):
             s = it % self.STAGES
             if it >= self.STAGES:
-                yield self.wait(f"EMPTY{s}", it // self.STAGES - 1)
-            writes = [(f"Q{s}", ("Q", it)), (f"dO{s}", ("dO", it)), (f"row{s}", ("row", it))]
-            self.async_ops.append(("tma", writes, f"FULL{s}"))
+                yield self.wait(f"EMPTYQ{s}", it // self.STAGES - 1)
+            writes = [(f"Q{s}", ("Q", it)), (f"row{s}", ("row", it))]
+            if not self.split_ring:
+                writes.append((f"dO{s}", ("dO", it)))
+            self.async_ops.append(("tma", writes, f"FULLQ{s}"))
         # the producer then waits for its loads to land (drain_wait): modelled by the loads
         # completing before the CTA ends, which the scheduler guarantees
+
+    def producer_do(self):
+        """The dO ring of the split case: the kernel's one producer thread polls both "empty"
+        barriers without blocking on either, which is two independent streams."""
+        for it in range(self.n):
+            s = it % self.STAGES
+            if it >= self.STAGES:
+                yield self.wait(f"EMPTYDO{s}", it // self.STAGES - 1)
+            self.async_ops.append(("tma", [(f"dO{s}", ("dO", it))], f"FULLDO{s}"))
 
     def mma_op(self, issuer, reads, writes):
         return ("mma", issuer, reads, writes)
@@ -141,9 +163,10 @@ class Model:
     def issuer_sd(self, who):
         """S and dP products: the single issuer's first part or warp 13 of the pair."""
         yield self.wait("KV", 0)
-        yield self.wait("FULL0", 0)
+        yield self.wait("FULLQ0", 0)
         yield self.gemm_s(who, 0, self.xb(0))
         yield self.commit(who, f"S_FULL{self.sp_slot(0)}")
+        yield self.wait("FULLDO0", 0)
         yield self.gemm_dp(who, 0, self.yb(0))
         yield self.commit(who, "DP_FULL")
 
@@ -156,12 +179,13 @@ class Model:
         for it in range(self.n):
             if it + 1 < self.n:
                 s1 = (it + 1) % self.STAGES
-                yield self.wait(f"FULL{s1}", (it + 1) // self.STAGES)
+                yield self.wait(f"FULLQ{s1}", (it + 1) // self.STAGES)
                 if it > 0:
                     yield self.wait(f"YFREE{self.yb(it - 1)}", (it - 1) // 3)
                 yield self.gemm_s("A", it + 1, self.xb(it + 1))
                 yield self.commit("A", f"S_FULL{self.sp_slot(it + 1)}")
                 yield self.wait("DQ_EMPTY", it)
+                yield self.wait(f"FULLDO{s1}", (it + 1) // self.STAGES)
                 yield self.gemm_dp("A", it + 1, self.xb(it))
                 yield self.commit("A", "DP_FULL")
         yield self.commit("A", "FINAL_A")
@@ -181,14 +205,17 @@ class Model:
             yield self.commit(who, "DQ_FULL")
             yield self.mma_op(who, [(Y, ("dS", it)), (f"Q{s}", ("Q", it))], [])            # dK
             yield self.commit(who, f"YFREE{self.yb(it)}" if self.NBUF == 3 else "G4")
-            yield self.commit(who, f"EMPTY{s}")
+            yield self.commit(who, f"EMPTYQ{s}")
+            if self.split_ring:
+                yield self.commit(who, f"EMPTYDO{s}")
             if single and it + 1 < self.n:
                 s1 = (it + 1) % self.STAGES
-                yield self.wait(f"FULL{s1}", (it + 1) // self.STAGES)
+                yield self.wait(f"FULLQ{s1}", (it + 1) // self.STAGES)
                 yield self.wait("G4", it)
                 yield self.gemm_s(who, it + 1, self.yb(it))
                 yield self.commit(who, f"S_FULL{self.sp_slot(it + 1)}")
                 yield self.wait("DQ_EMPTY", it)
+                yield self.wait(f"FULLDO{s1}", (it + 1) // self.STAGES)
                 yield self.gemm_dp(who, it + 1, self.xb(it))
                 yield self.commit(who, "DP_FULL")
         yield self.commit(who, "ACC")
@@ -199,7 +226,7 @@ class Model:
         for it in range(self.n):
             s = it % self.STAGES
             X, Y = f"buf{self.xb(it)}", f"buf{self.yb(it)}"
-            yield self.wait(f"FULL{s}", it // self.STAGES)
+            yield self.wait(f"FULLQ{s}", it // self.STAGES)  # Q with the lse2 / D rows
             yield self.wait(f"S_FULL{self.sp_slot(it)}", self.sp_phase(it))
             self.expect(f"row{s}", ("row", it))        # LSE row
             self.expect(X, ("S", it))
@@ -231,7 +258,7 @@ class Model:
             yield ("wait_async", h1)
             yield self.arrive(f"DS_EMPTY{self.dt(it)}")
             yield ("wait_async", h2)
-            yield self.arrive(f"EMPTY{s}")
+            yield self.arrive(f"EMPTYDO{s}")
         else:
             yield ("wait_async", h1)
             yield self.arrive(f"DS_EMPTY{self.dt(it)}")
@@ -270,6 +297,8 @@ class Model:
 
     def make_roles(self):
         roles = {"producer": self.producer(), "softmax": self.softmax(), "drain": self.drain()}
+        if self.split_ring:
+            roles["producer_do"] = self.producer_do()
         if self.n > 0:
             if self.split:
                 roles["mma_a"] = self.issuer_a()
@@ -628,3 +657,194 @@ def test_forward_model_catches_one_shared_pv_barrier():
         except ProtocolError:
             caught += 1
     assert caught > 0
+
+
+class PersistentFwdModel(FwdModel):
+    """One CTA of the persistent forward (csrc/fwd_sm103.cu, fwd_sm103_persistent_kernel) over a
+    list of items, each with its number of key tiles (0 for an item whose rows see no key, which
+    every role skips).  The producer thread's two polled streams (Q tiles, gated on the S issuer's
+    commit after an item's last S product; K / V tiles through the ring, running on into the next
+    item) are two actors here.  The P V issuer commits "O full" after an item's last product and
+    waits for "O free" (the softmax warps have read O) before the next item's first product, which
+    overwrites O.  Per-item barriers count the items with work, per-tile ones all key tiles."""
+
+    def __init__(self, items, d, rng):
+        super().__init__(sum(items), d, rng)
+        self.items = items
+        for name in ("QE", "OFULL", "OFREE"):
+            self.bars[name] = Bar(name, 1)
+        self.res = {"O": None}
+
+    def active(self):
+        return [(k, c) for k, c in enumerate(self.items) if c > 0]
+
+    def make_roles(self):
+        roles = {"tma_q": self.p_q(), "tma_kv": self.p_kv(), "softmax": self.p_softmax()}
+        if self.n > 0:
+            roles["s_issuer"] = self.p_s()
+            roles["pv_issuer"] = self.p_pv()
+        return roles
+
+    def p_q(self):
+        for a, (k, _) in enumerate(self.active()):
+            if a > 0:
+                yield self.wait("QE", a - 1)
+            self.async_ops.append(("tma", [("Qt", ("Q", k))], "Q"))
+
+    def p_kv(self):
+        jg = 0
+        for _, c in self.active():
+            for _ in range(c):
+                st = jg % self.STAGES
+                if jg >= self.STAGES:
+                    yield self.wait(f"EMPTY{st}", jg // self.STAGES - 1)
+                self.async_ops.append(("tma", [(f"K{st}", ("K", jg)), (f"V{st}", ("V", jg))], f"FULL{st}"))
+                jg += 1
+
+    def p_s(self):
+        jg = 0
+        for a, (k, c) in enumerate(self.active()):
+            yield self.wait("Q", a)
+            for _ in range(c):
+                st, b = jg % self.STAGES, jg % self.NB
+                yield self.wait(f"FULL{st}", jg // self.STAGES)
+                if jg >= self.NB:
+                    yield self.wait(f"PV{b}", jg // self.NB - 1)
+                yield ("mma", "S", [("Qt", ("Q", k)), (f"K{st}", ("K", jg))], [(f"sbuf{b}", ("S", jg))])
+                yield ("commit", "S", f"S{b}")
+                jg += 1
+            yield ("commit", "S", "QE")
+
+    def p_pv(self):
+        jg = 0
+        for a, (k, c) in enumerate(self.active()):
+            for j in range(c):
+                st, b = jg % self.STAGES, jg % self.NB
+                yield self.wait(f"P{b}", jg // self.NB)
+                if j == 0 and a > 0:
+                    yield self.wait("OFREE", a - 1)
+                yield ("mma_pv", "PV", jg, b, st, k, j)
+                yield ("commit", "PV", f"PV{b}")
+                yield ("commit", "PV", f"EMPTY{st}")
+                jg += 1
+            yield ("commit", "PV", "OFULL")
+        yield ("commit", "PV", "FINAL")
+        yield self.wait("FINAL", 0)
+
+    def p_softmax(self):
+        jg, a = 0, 0
+        for k, c in enumerate(self.items):
+            for j in range(c):
+                b = jg % self.NB
+                yield self.wait(f"S{b}", jg // self.NB)
+                self.expect(f"sbuf{b}", ("S", jg))
+                yield self.STEP
+                self.put(f"sbuf{b}", ("P", jg))
+                if j > 0 and self.rng.random() < 0.5:  # the running max moved: rescale O
+                    yield self.wait(f"PV{(jg - 1) % self.NB}", (jg - 1) // self.NB)
+                    self.expect("O", (k, j))
+                    yield self.STEP
+                    self.expect("O", (k, j))
+                yield self.arrive(f"P{b}")
+                jg += 1
+            if c > 0:  # epilogue: read O, then let the next item's first P V product in
+                yield self.wait("OFULL", a)
+                self.expect("O", (k, c))
+                yield self.STEP
+                self.expect("O", (k, c))
+                yield self.arrive("OFREE")
+                a += 1
+
+    def exec_mma(self, who):
+        op = self.mma_q[who][0]
+        if op[0] == "mma_pv":
+            self.mma_q[who].pop(0)
+            _, _, jg, b, st, k, j = op
+            self.expect(f"sbuf{b}", ("P", jg))
+            self.expect(f"V{st}", ("V", jg))
+            if j > 0:
+                self.expect("O", (k, j))
+            self.put("O", (k, j + 1))
+            return
+        Model.exec_mma(self, who)
+
+
+def _random_items(rng):
+    return [rng.choice([0, 1, 1, 2, 3, 4, 6]) for _ in range(rng.choice([1, 2, 3, 4, 6]))]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_persistent_forward_protocol_sound_under_random_schedules(d):
+    rng = random.Random(3000 + d)
+    for _ in range(400):
+        PersistentFwdModel(_random_items(rng), d, random.Random(rng.random())).run()
+
+
+def _persistent_fails(model_cls, d=128, trials=400, seed=17):
+    rng = random.Random(seed)
+    for _ in range(trials):
+        try:
+            model_cls([3, 0, 2, 4, 1], d, random.Random(rng.random())).run()
+        except ProtocolError:
+            return True
+    return False
+
+
+def test_persistent_forward_o_free_is_implied_by_the_next_p():
+    # the next item's first P V product also waits for that item's first P, which the softmax
+    # warps produce only after their epilogue has read O: the "O free" wait the kernel keeps (it
+    # names the dependency) is implied, and the model agrees that dropping it is no error
+    class NoOFree(PersistentFwdModel):
+        def p_pv(self):
+            for req in super().p_pv():
+                if req[0] == "wait" and req[1] == "OFREE":
+                    continue
+                yield req
+
+    assert not _persistent_fails(NoOFree, trials=100)
+
+
+def test_persistent_forward_model_catches_an_o_read_after_the_next_p():
+    # an epilogue that read O only after producing the next item's first P (a reordering the
+    # kernel must not make) lets the next item's first P V product overwrite O: with the "O free"
+    # wait dropped too, the model finds it
+    class LateRead(PersistentFwdModel):
+        def p_pv(self):
+            for req in super().p_pv():
+                if req[0] == "wait" and req[1] == "OFREE":
+                    continue
+                yield req
+
+        def p_softmax(self):
+            jg, a, pending = 0, 0, None
+            for k, c in enumerate(self.items):
+                for j in range(c):
+                    b = jg % self.NB
+                    yield self.wait(f"S{b}", jg // self.NB)
+                    self.expect(f"sbuf{b}", ("S", jg))
+                    yield self.STEP
+                    self.put(f"sbuf{b}", ("P", jg))
+                    yield self.arrive(f"P{b}")
+                    jg += 1
+                    if pending is not None:  # the previous item's O read, too late
+                        yield self.STEP
+                        self.expect("O", pending)
+                        pending = None
+                if c > 0:
+                    yield self.wait("OFULL", a)
+                    pending = (k, c)
+                    a += 1
+
+    assert _persistent_fails(LateRead)
+
+
+def test_persistent_forward_model_catches_an_early_q_load():
+    # the next item's Q tile loaded before the S products of this item have read Q
+    class NoQe(PersistentFwdModel):
+        def p_q(self):
+            for req in super().p_q():
+                if req[0] == "wait" and req[1] == "QE":
+                    continue
+                yield req
+
+    assert _persistent_fails(NoQe)
