@@ -589,8 +589,11 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
             // dS = P * (dP - D): packed in place into this warp's first 32 columns of Y for
             // the dK product, and into the shared dS tile for dQ.
             if (!(ok = wait_bar_warp(bar(B_DP_FULL), it & 1, abort_flag, p.err))) break;
-            // the dS tile of this iteration was last used NDS iterations ago
-            if (it >= NDS &&
+            // The dS tile of this iteration was last used NDS iterations ago.  At d = 128 its
+            // release is waited for only just before the stores below, so the dP load and the
+            // arithmetic overlap the wait (measured 335 -> 331 us on the bench shape, 1193 ->
+            // 1165 us on fp16 S = 8192; at d = 64 it made no gain and stays here).
+            if (D != 128 && it >= NDS &&
                 !(ok = wait_bar_warp(bar(B_DS_EMPTY + dt(it)), ((it - NDS) / NDS) & 1, abort_flag, p.err)))
                 break;
             ptx::tc_fence_after();
@@ -616,6 +619,11 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
                     pk[q / 2 + 1] = pack2<kBF16>(s23.x, s23.y);
                 }
                 ptx::tmem_st32(Y, pk);  // columns already read
+                if (D == 128 && it >= NDS &&
+                    !(ok = wait_bar_warp(bar(B_DS_EMPTY + dt(it)), ((it - NDS) / NDS) & 1, abort_flag, p.err))) {
+                    ptx::tmem_wait_st();  // no TMEM store in flight at the release
+                    break;
+                }
 #pragma unroll
                 for (int u = 0; u < kHalfQ / 8; ++u)  // 8 queries = one 16-byte chunk
                     *reinterpret_cast<uint4*>(sdS_row + dt(it) * C::kdS_B + ((u ^ (t & 7)) << 4)) =
