@@ -211,6 +211,32 @@ def test_forward_helper(dt, causal, S_q, S_k, d):
         assert float(np.max(np.abs(lse[fin] - L64[fin]))) <= 1e-4
 
 
+@pytest.mark.parametrize("dt,B,H,H_kv,S_q,S_k,d,causal,win", [
+    # more query tiles than SMs: the persistent forward (256-row items of two query tiles);
+    # ragged last items (the second tile partly or wholly past S_q), rows that see no key
+    # (S_q > S_k, causal), keys past the queries, sliding windows, both head dims
+    ("bf16", 2, 16, 4, 2300, 2300, 128, True, 0),
+    ("f16", 2, 32, 8, 1100, 1500, 64, True, 0),
+    ("bf16", 1, 32, 8, 1500, 1100, 128, True, 0),
+    ("bf16", 1, 32, 8, 2200, 2200, 128, True, 300),
+    ("f16", 2, 16, 16, 1130, 1130, 64, True, 100),
+    ("bf16", 1, 48, 16, 1200, 1200, 96, True, 0),
+    ("bf16", 1, 32, 8, 2000, 2000, 128, False, 500)])
+def test_forward_persistent_path(dt, B, H, H_kv, S_q, S_k, d, causal, win):
+    w = Workload("fwd_persistent", dt, B, H, H_kv, S_q, S_k, d, causal, seed=S_q + 7 * S_k + win, window=win)
+    Q, K, V, _ = make_inputs(w)
+    O, LSE = fa.fa_fwd(Q.cuda(), K.cuda(), V.cuda(), scale=w.scale, causal=causal, window_size=win)
+    torch.cuda.synchronize()
+    fa.fa_check_device()
+    O64, L64 = oracle.ref_fwd(f64(Q), f64(K), f64(V), w.scale, causal, win)
+    assert bool(torch.isfinite(O).all())
+    assert rel_err(f64(O), O64) <= TOL[dt]
+    lse, fin = f64(LSE), np.isfinite(L64)
+    assert bool(np.all(np.isneginf(lse[~fin]))) and bool(np.all(np.isfinite(lse[fin])))
+    if fin.any():
+        assert float(np.max(np.abs(lse[fin] - L64[fin]))) <= 1e-4
+
+
 def test_host_buffer_entry_point_matches_device():
     w = Workload("host", "bf16", 1, 4, 2, 256, 256, 64, True, seed=6)
     Q, K, V, dO, O, LSE = prepare(w)
