@@ -185,6 +185,7 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
     // not wait until TMA has read that out.  At d = 64 both tiles of an iteration share one
     // full and one empty barrier (measured 3 % faster there).
     constexpr bool kSplitRing = D == 128;
+    constexpr bool kPipeLd = D == 128;  // softmax passes: TMEM loads in two halves, overlapped
     auto full_q = [&](int s) { return bar(B_STAGE0 + s); };
     auto empty_q = [&](int s) { return bar(B_STAGE0 + C::STAGES + s); };
     auto full_do = [&](int s) { return kSplitRing ? bar(B_STAGE0 + 2 * C::STAGES + s) : full_q(s); };
@@ -549,13 +550,21 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
             // chains stay one basic block.
             uint32_t Pp[kHalfQ / 2];
             auto p_block = [&](bool masked) {
+                // d = 128: the second 32 columns load while the first 32 are computed (bench
+                // shape 331 -> 329 us; at d = 64 it measured 241 -> 243 us and is not used)
                 uint32_t r[kHalfQ];
                 ptx::tmem_ld32p(X, r);
-                ptx::tmem_ld32p(X + 32, r + 32);
-                ptx::tmem_wait_ld();
+                if constexpr (kPipeLd) {
+                    ptx::tmem_wait_ld_regs(r);
+                    ptx::tmem_ld32p(X + 32, r + 32);
+                } else {
+                    ptx::tmem_ld32p(X + 32, r + 32);
+                    ptx::tmem_wait_ld();
+                }
                 const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
                 for (int q = 0; q < kHalfQ; q += 4) {
+                    if (kPipeLd && q == 32) ptx::tmem_wait_ld_regs(r + 32);
                     const float4 l4 = *reinterpret_cast<const float4*>(sl + q);
                     float2 a = __ffma2_rn(make_float2(__uint_as_float(r[q]), __uint_as_float(r[q + 1])), sc2,
                                           make_float2(-l4.x, -l4.y));
@@ -598,13 +607,20 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
                 break;
             ptx::tc_fence_after();
             {
+                // as in the P pass (d = 128)
                 uint32_t r[kHalfQ];
                 ptx::tmem_ld32p(Y, r);
-                ptx::tmem_ld32p(Y + 32, r + 32);
-                ptx::tmem_wait_ld();
+                if constexpr (kPipeLd) {
+                    ptx::tmem_wait_ld_regs(r);
+                    ptx::tmem_ld32p(Y + 32, r + 32);
+                } else {
+                    ptx::tmem_ld32p(Y + 32, r + 32);
+                    ptx::tmem_wait_ld();
+                }
                 uint32_t pk[kHalfQ / 2];
 #pragma unroll
                 for (int q = 0; q < kHalfQ; q += 4) {
+                    if (kPipeLd && q == 32) ptx::tmem_wait_ld_regs(r + 32);
                     const float4 d4 = *reinterpret_cast<const float4*>(sd + q);
                     const float2 p01 = unpack2<kBF16>(Pp[q / 2]);
                     const float2 p23 = unpack2<kBF16>(Pp[q / 2 + 1]);
