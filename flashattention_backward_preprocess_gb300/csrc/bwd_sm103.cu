@@ -160,6 +160,20 @@ __device__ __forceinline__ float2 unpack2(uint32_t v) {
     return __half22float2(*reinterpret_cast<__half2*>(&v));
 }
 
+// tcgen05.wait::ld that also names the 32 registers a tcgen05.ld filled as operands, so the
+// compiler cannot move a use of them above the wait (they are written asynchronously).
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t* r) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+                   "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]),
+                   "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]),
+                   "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]),
+                   "+r"(r[31])
+                 :
+                 : "memory");
+}
+
 static_assert(B_STAGE0 == 23, "Cfg::kNumBars counts 23 named barriers before the stage ring");
 
 template <typename T, int D, bool kDet, int kSplit>
@@ -555,7 +569,7 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
                 uint32_t r[kHalfQ];
                 ptx::tmem_ld32p(X, r);
                 if constexpr (kPipeLd) {
-                    ptx::tmem_wait_ld_regs(r);
+                    tmem_wait_ld_regs(r);
                     ptx::tmem_ld32p(X + 32, r + 32);
                 } else {
                     ptx::tmem_ld32p(X + 32, r + 32);
@@ -564,7 +578,7 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
                 const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
                 for (int q = 0; q < kHalfQ; q += 4) {
-                    if (kPipeLd && q == 32) ptx::tmem_wait_ld_regs(r + 32);
+                    if (kPipeLd && q == 32) tmem_wait_ld_regs(r + 32);
                     const float4 l4 = *reinterpret_cast<const float4*>(sl + q);
                     float2 a = __ffma2_rn(make_float2(__uint_as_float(r[q]), __uint_as_float(r[q + 1])), sc2,
                                           make_float2(-l4.x, -l4.y));
@@ -611,7 +625,7 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
                 uint32_t r[kHalfQ];
                 ptx::tmem_ld32p(Y, r);
                 if constexpr (kPipeLd) {
-                    ptx::tmem_wait_ld_regs(r);
+                    tmem_wait_ld_regs(r);
                     ptx::tmem_ld32p(Y + 32, r + 32);
                 } else {
                     ptx::tmem_ld32p(Y + 32, r + 32);
@@ -620,7 +634,7 @@ __global__ void __launch_bounds__(threads_for(kDet, D), 1)
                 uint32_t pk[kHalfQ / 2];
 #pragma unroll
                 for (int q = 0; q < kHalfQ; q += 4) {
-                    if (kPipeLd && q == 32) ptx::tmem_wait_ld_regs(r + 32);
+                    if (kPipeLd && q == 32) tmem_wait_ld_regs(r + 32);
                     const float4 d4 = *reinterpret_cast<const float4*>(sd + q);
                     const float2 p01 = unpack2<kBF16>(Pp[q / 2]);
                     const float2 p23 = unpack2<kBF16>(Pp[q / 2 + 1]);

@@ -209,19 +209,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
         "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
 }
-// tcgen05.wait::ld that also names the 32 registers a tcgen05.ld filled as operands, so the
-// compiler cannot move a use of them above the wait (they are written asynchronously).
-__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t* r) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
-                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
-                   "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]),
-                   "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]),
-                   "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]),
-                   "+r"(r[31])
-                 :
-                 : "memory");
-}
 // 32 lanes x 32 columns load into a register array slice.
 __device__ __forceinline__ void tmem_ld32p(uint32_t taddr, uint32_t* r) {
     asm volatile(
